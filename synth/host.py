@@ -1,0 +1,86 @@
+"""Host-side (numpy) draws of the workloads' tensors, by counter.
+
+Any table row, scale or residual element can be drawn on its own, so the
+oracle side can regenerate exactly the rows it needs while the device twin
+(``synth/device.py``) fills whole tables of tens of GB in HBM.
+"""
+
+import functools
+
+import numpy as np
+
+from .configs import (
+    N_TABLES,
+    ROW_BYTES,
+    STREAM_G,
+    STREAM_H,
+    STREAM_SCALE,
+    STREAM_TABLE,
+    STREAM_W,
+)
+from .philox import philox4x64, philox_u32
+from .sampler import bf16_normal_table, e4m3_normal_table, sample_codes, scale_from_u32
+
+W_SIGMA = 1.0 / np.sqrt(512.0)
+
+
+@functools.lru_cache(maxsize=None)
+def e4m3_table():
+    return e4m3_normal_table(1.0)
+
+
+@functools.lru_cache(maxsize=None)
+def bf16_table(sigma):
+    return bf16_normal_table(float(sigma))
+
+
+def table_rows(seed, j, row):
+    """e4m3 code bytes uint8 [n, 256] of rows (j[i], row[i])."""
+    j = np.asarray(j, dtype=np.uint64).reshape(-1)
+    row = np.asarray(row, dtype=np.uint64).reshape(-1)
+    blocks = row[:, None] * np.uint64(ROW_BYTES // 8) + np.arange(ROW_BYTES // 8, dtype=np.uint64)[None, :]
+    out = philox4x64(blocks, 0, 0, 0, np.uint64(seed), (np.uint64(STREAM_TABLE) + j)[:, None])
+    u = out.reshape(len(row), -1).view(np.uint32)  # little-endian: low half first
+    return sample_codes(e4m3_table(), u).astype(np.uint8).reshape(len(row), ROW_BYTES)
+
+
+def scales(seed, j, row):
+    """fp32 scales [n] of rows (j[i], row[i])."""
+    j = np.asarray(j, dtype=np.uint64).reshape(-1)
+    row = np.asarray(row, dtype=np.uint64).reshape(-1)
+    u = philox_u32(np.uint64(seed), np.uint64(STREAM_SCALE) + j, row)
+    return scale_from_u32(u)
+
+
+def full_tables(seed, R):
+    """Whole tables uint8 [48, R, 256] and scales fp32 [48, R] (small R only)."""
+    jj = np.repeat(np.arange(N_TABLES), R)
+    rr = np.tile(np.arange(R), N_TABLES)
+    t = table_rows(seed, jj, rr).reshape(N_TABLES, R, ROW_BYTES)
+    s = scales(seed, jj, rr).reshape(N_TABLES, R)
+    return t, s
+
+
+def bf16_words(seed, stream, sigma, word0, count):
+    """bf16 bit patterns uint16 [count] of words word0.. of a stream."""
+    w = np.uint64(word0) + np.arange(count, dtype=np.uint64)
+    u = philox_u32(np.uint64(seed), np.uint64(stream), w)
+    return sample_codes(bf16_table(sigma), u).astype(np.uint16)
+
+
+def h_rows(seed, d, t_idx):
+    """Residual rows h bf16 bits [n, d] of query tokens t_idx (N(0,1))."""
+    t_idx = np.asarray(t_idx, dtype=np.uint64).reshape(-1)
+    w = t_idx[:, None] * np.uint64(d) + np.arange(d, dtype=np.uint64)[None, :]
+    u = philox_u32(np.uint64(seed), np.uint64(STREAM_H), w)
+    return sample_codes(bf16_table(1.0), u).astype(np.uint16).reshape(len(t_idx), d)
+
+
+def w_out(seed, d):
+    """W_out bf16 bits [512, d], N(0, 1/512)."""
+    return bf16_words(seed, STREAM_W, W_SIGMA, 0, 512 * d).reshape(512, d)
+
+
+def g_vec(seed, d):
+    """Gate vector g bf16 bits [d], N(0, 1)."""
+    return bf16_words(seed, STREAM_G, 1.0, 0, d)

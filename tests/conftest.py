@@ -1,0 +1,19 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+    config.addinivalue_line("markers", "slow: full-size workloads (tens of GB on the device)")
+
+
+def pytest_collection_modifyitems(config, items):
+    # A GPU test on a machine without a GPU is a failure to set up, not a skip,
+    # unless the run deselected GPU tests with -m "not gpu".
+    pass
