@@ -1,0 +1,470 @@
+"""Benchmark of the Engram memory read (hash + gather + fuse) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch of the workload:
+engram_hash -> engram_gather_reduce -> engram_fuse through the C ABI (the
+same kernels engram_forward launches), h updated in place.  Inputs are
+resident in HBM when the timed region starts and are larger than L2 (tables
+of 13-103 GB, h of 0.5-2 GB), so no L2 flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  For N > 1 (torchrun, one rank per GPU) every
+rank runs its own batch of the workload on replicated tables: the path
+shards over tokens with no collective ("weak" scaling).
+
+--impl reference times the CPU oracle (the plain C definition) on the host
+cores over a bounded sample of the same workload and prints the same line.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Engram tokens/sec (hash+gather+fuse) and achieved GB/s vs HBM/host-link roofline"
+UNIT = "tokens/s"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# Algorithmic bytes per query token of each kernel (what the method must move):
+#   hash:   4 B of token id in, 48 x 8 B of row index out
+#   gather: 48 x 256 B of rows + 48 x 4 B of scales + 384 B of idx in, 512 x 4 B of mem out
+#   fuse:   512 x 4 B of mem in, d x 2 B of h in, d x 2 B of h out
+def kernel_bytes_per_token(d):
+    return {"hash": 4 + 48 * 8, "gather": 48 * 256 + 48 * 4 + 48 * 8 + 512 * 4, "fuse": 512 * 4 + 4 * d}
+
+
+def nominal_bytes_per_token(d):
+    """The path's nominal bytes: 48 rows of 256 B plus the residual read and write."""
+    return 48 * 256 + 4 * d
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "engram_gram_hash_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload, units):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    if there is none for the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel, {})
+    if e.get("source_hash") != kernel_source_hash() or "bytes_per_token" not in e:
+        return None
+    return e["bytes_per_token"] * units
+
+
+def smi_index(local_rank):
+    """nvidia-smi's name for this rank's GPU (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        items = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(items):
+            return items[local_rank]
+    return str(local_rank)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"engram_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm ----
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import engram_gram_hash_gb300 as eg
+    from synth import device as sd
+    from synth.configs import CONFIGS, default_seeds, make_tokens
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    eg.lib()
+    base = CONFIGS[args.workload]
+    # weak scaling: rank r draws its own token batch (tables are replicated weights)
+    cfg = base.with_(seed=base.seed) if rank == 0 else base.with_(seed=base.seed + 1000 * rank)
+    seeds = default_seeds()
+    c = eg.make_config(cfg.V, cfg.R, cfg.d, seeds, cfg.rms_eps)
+    tok, offs = make_tokens(cfg)
+    tokens = torch.from_numpy(tok).to(dev)
+    seq_offsets = torch.from_numpy(offs).to(dev)
+    if cfg.host_tables:
+        tables = torch.empty((48, cfg.R, 256), dtype=torch.uint8, pin_memory=True)
+        scales = torch.empty((48, cfg.R), dtype=torch.float32, pin_memory=True)
+    else:
+        tables = torch.empty((48, cfg.R, 256), dtype=torch.uint8, device=dev)
+        scales = torch.empty((48, cfg.R), dtype=torch.float32, device=dev)
+    sd.fill_tables(tables, base.seed)
+    sd.fill_scales(scales, base.seed)
+    W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=dev)
+    g = torch.empty(cfg.d, dtype=torch.bfloat16, device=dev)
+    h = torch.empty((cfg.tq, cfg.d), dtype=torch.bfloat16, device=dev)
+    sd.fill_w_out(W, base.seed)
+    sd.fill_g(g, base.seed)
+    sd.fill_h(h, cfg.seed)
+    nq = cfg.tq
+    idx = torch.empty((nq, 48), dtype=torch.int64, device=dev)
+    mem = torch.empty((nq, 512), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    host = cfg.host_tables
+    if host:
+        cap = nq * 48
+        fws = torch.empty(eg.engram_forward_host_workspace_bytes(c, nq, cap), dtype=torch.uint8, device=dev)
+        n_unique = torch.zeros(1, dtype=torch.int64, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        ev_a, ev_b = torch.cuda.Event(), torch.cuda.Event()
+
+    def step(ev=None):
+        if host:
+            eg.engram_forward_host(c, tokens, seq_offsets, tables, scales, W, g, h, cap, last_n=cfg.last_n,
+                                   n_query=nq, workspace=fws, n_unique=n_unique, side_stream=side, ev_dedup=ev_a,
+                                   ev_staged=ev_b)
+            return 1
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash(c, tokens, seq_offsets, last_n=cfg.last_n, n_query=nq, idx=idx)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_gather_reduce(c, tables, scales, idx, mem=mem)
+        if ev is not None:
+            ev[2].record(stream)
+        eg.engram_fuse(c, mem, W, g, h)
+        if ev is not None:
+            ev[3].record(stream)
+        return 3
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if eg.engram_last_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(smi_index(local_rank)) as cs:
+        t0.record(stream)
+        for k in range(K):
+            launches += step(None if host else evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1)
+    status = eg.engram_last_error()
+    if status != 0:
+        raise RuntimeError(f"device error {status} in the timed region")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    clocks = cs.summary()
+
+    peaks = measured_peaks()
+    per_kernel_ms = {}
+    if not host:
+        per_kernel_ms = {
+            "hash": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
+            "gather": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
+            "fuse": sum(e[2].elapsed_time(e[3]) for e in evs) / K,
+        }
+    kb = kernel_bytes_per_token(cfg.d)
+    kernels = {}
+    for name, kms in per_kernel_ms.items():
+        gbs = kb[name] * nq / (kms * 1e-3) / 1e9
+        kernels[name] = {"ms": round(kms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 3)}
+    roofline = None
+    if per_kernel_ms:
+        dom = max(per_kernel_ms, key=per_kernel_ms.get)
+        ach = kb[dom] * nq / (per_kernel_ms[dom] * 1e-3) / 1e9
+        tr = ncu_traffic(dom, args.workload, nq)
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": tr,
+                    "algorithmic_bytes_per_launch": kb[dom] * nq,
+                    "peak_src": f"{peaks['src']} hbm_gbs (burst copy)"}
+
+    tokens_total = nq * world
+    value = tokens_total / (ms_max * 1e-3 / K)
+    step_gbs = nominal_bytes_per_token(cfg.d) * nq / (ms_max * 1e-3 / K) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3->f32 gather, bf16 x bf16 -> f32 projection, bf16 residual",
+        "data": "synthetic (seeded; tables e4m3 ~ quantised N(0,1), per-row fp32 scales U[0.5,2])",
+        "config": {"workload": args.workload, "V": cfg.V, "R": cfg.R, "n_seqs": cfg.n_seqs,
+                   "tokens_per_step_per_gpu": cfg.t_all, "query_tokens_per_step_per_gpu": nq, "d_model": cfg.d,
+                   "table_bytes": cfg.table_bytes, "tables_in": "pinned host" if host else "HBM",
+                   "token_ids": ("uniform" if cfg.zipf_s == 0 else f"Zipf({cfg.zipf_s})"),
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world} (replicated tables)"},
+        "step_roofline": {"nominal_bytes_per_token": nominal_bytes_per_token(cfg.d), "achieved_GBps": round(step_gbs, 1),
+                          "peak_GBps": peaks["hbm_gbs"], "frac": round(step_gbs / peaks["hbm_gbs"], 4)},
+        "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
+    }
+    if host:
+        out["config"]["n_unique_rows"] = int(n_unique.item())
+    out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    return out
+
+
+def e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h_dev, nq, dev, world):
+    """Same metric through the public API with host buffers: every step copies
+    the step's tokens, offsets and residual h from pinned host memory to the
+    device, runs engram_forward, and reads h back to pinned host memory."""
+    import torch
+    import torch.distributed as dist
+
+    tok_h = tokens.cpu().pin_memory()
+    off_h = seq_offsets.cpu().pin_memory()
+    h_in = h_dev.cpu().pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    tok_d, off_d, h_d = torch.empty_like(tokens), torch.empty_like(seq_offsets), torch.empty_like(h_dev)
+    stream = torch.cuda.current_stream()
+    if cfg.host_tables:
+        cap = nq * 48
+        ws = torch.empty(eg.engram_forward_host_workspace_bytes(c, nq, cap), dtype=torch.uint8, device=dev)
+        nu = torch.zeros(1, dtype=torch.int64, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        ea, eb = torch.cuda.Event(), torch.cuda.Event()
+    else:
+        ws = torch.empty(eg.engram_forward_workspace_bytes(c, nq), dtype=torch.uint8, device=dev)
+
+    def one():
+        tok_d.copy_(tok_h, non_blocking=True)
+        off_d.copy_(off_h, non_blocking=True)
+        h_d.copy_(h_in, non_blocking=True)
+        if cfg.host_tables:
+            eg.engram_forward_host(c, tok_d, off_d, tables, scales, W, g, h_d, cap, last_n=cfg.last_n, n_query=nq,
+                                   workspace=ws, n_unique=nu, side_stream=side, ev_dedup=ea, ev_staged=eb)
+        else:
+            eg.engram_forward(c, tok_d, off_d, tables, scales, W, g, h_d, last_n=cfg.last_n, n_query=nq, workspace=ws)
+        h_out.copy_(h_d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    a.record(stream)
+    for _ in range(K):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    h2d = tok_h.numel() * 4 + off_h.numel() * 8 + h_in.numel() * 2
+    d2h = h_out.numel() * 2
+    return {"value": round(nq * world / (ms * 1e-3 / K), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / K, 4), "api": "engram_forward"}
+
+
+# --------------------------------------------------------- the CPU oracle ---
+
+
+def oracle_sample_tokens_per_s(cfg, seconds, seed=0):
+    """Run the CPU oracle (hash + gather + fuse) on a sample of query tokens
+    of the workload, growing the sample until it takes ~`seconds` of CPU.
+    Rows, scales and h for the sample are drawn on the host beforehand and
+    are not timed.  Returns (tokens/s, n_tokens, seconds)."""
+    import oracle
+    from synth import host
+    from synth.configs import default_seeds, make_tokens, query_positions
+
+    tok, offs = make_tokens(cfg)
+    qpos = query_positions(cfg, offs)
+    seeds = default_seeds()
+    W = host.w_out(cfg.seed, cfg.d)
+    g = host.g_vec(cfg.seed, cfg.d)
+    rng = np.random.default_rng(seed)
+    n = 16
+    done_t, done_s = 0, 0.0
+    while True:
+        q = np.sort(rng.choice(cfg.tq, size=min(n, cfg.tq), replace=False))
+        pos = qpos[q]
+        # draw the inputs the oracle needs (untimed): rows for the oracle's own idx
+        idx0 = oracle.hash_positions(tok, offs, cfg.V, cfg.R, seeds, pos)
+        jj = np.tile(np.arange(48), len(q))
+        rows = host.table_rows(cfg.seed, jj, idx0.reshape(-1)).reshape(len(q), 48, 256)
+        sc = host.scales(cfg.seed, jj, idx0.reshape(-1)).reshape(len(q), 48)
+        h0 = host.h_rows(cfg.seed, cfg.d, q)
+        t0 = time.perf_counter()
+        idx = oracle.hash_positions(tok, offs, cfg.V, cfg.R, seeds, pos)
+        mem = oracle.gather_reduce_rows(rows, sc)
+        oracle.fuse(mem, W, g, h0, cfg.rms_eps)
+        dt = time.perf_counter() - t0
+        assert np.array_equal(idx, idx0)
+        done_t += len(q)
+        done_s += dt
+        if done_s >= seconds or len(q) == cfg.tq:
+            break
+        n = min(cfg.tq, max(n * 2, int(n * seconds / max(dt, 1e-3) * 0.5)))
+    return done_t / done_s, done_t, done_s
+
+
+def cpu_baseline(cfg, seconds):
+    v, n, s = oracle_sample_tokens_per_s(cfg, seconds)
+    return {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} query tokens of the {cfg.name} workload drawn at random ({s:.1f} s single-threaded; "
+                      "hash + gather + fuse, input draws untimed)"}
+
+
+def run_reference(args, rank, world):
+    from synth.configs import CONFIGS
+
+    cfg = CONFIGS[args.workload]
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample_tokens_per_s(cfg, 0.2)
+    total_t, total_s = 0, 0.0
+    for k in range(args.steps):
+        v, n, s = oracle_sample_tokens_per_s(cfg, per_step, seed=k + 1)
+        total_t += n
+        total_s += s
+    value = total_t / total_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+        "data": "synthetic (seeded)", "config": {"workload": args.workload, "V": cfg.V, "R": cfg.R, "d_model": cfg.d,
+                                                  "query_tokens_per_step_per_gpu": cfg.tq},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{total_t} query tokens over {args.steps} steps, single-threaded, "
+                                   "each step a random sample of the workload"},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="large", choices=["tiny", "decode", "prefill", "large", "host"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3  # at least three warm-up steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,875 @@
+// libengram: n-gram hash, row gather/dequant/reduce, dedup and host-row
+// staging kernels, and their C entry points.
+//
+// Sources: vramglass.com "deepseek-v4-1-flash-local-deployment", section
+// "What makes up the 511 GB of weights?" (2/3/4-gram hash tables, two modules
+// of 8 heads, 48 rows of ~12 KB per token, token-only addresses prefetched in
+// one batch); rohitghumare.com "guides/deepseek-v4-1-flash", section "Engram:
+// the table that is never multiplied" (suffix n-grams, one row per (order,
+// head), 256-byte FP8 rows, host tables read over unified addressing on a
+// side stream, bitwise-identical host-table mode).
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "fuse.cuh"
+
+namespace engram {
+
+// ===================================================================== hash ==
+// One thread per (query token, table): 48 consecutive threads share a token,
+// so the 2-4 token loads hit L1 and the int64 idx writes are coalesced.
+
+struct HashParams {
+    const int32_t *tokens;
+    const int64_t *offs;
+    int64_t n_seqs;
+    int64_t n_query;
+    uint64_t R;
+    uint64_t rmask;  // R-1 when R is a power of two
+    int32_t V;
+    int32_t last_n;
+    int32_t pow2;
+    uint64_t seeds[kTables];
+};
+
+// Row index of table j for the token at global position p of a sequence that
+// starts at `start` (earlier positions read the pad id V).
+__device__ __forceinline__ int64_t hash_one(const HashParams &a, uint64_t seed, int j, int64_t start, int64_t p,
+                                            bool &bad) {
+    const int n = 2 + (j % kTablesPerModule) / 8;  // order of table j
+    uint64_t h = seed;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i < n) {
+            const int64_t q = p - (n - 1) + i;  // oldest id first
+            int32_t id = a.V;
+            if (q >= start) {
+                id = __ldg(a.tokens + q);
+                if (id < 0 || id >= a.V) bad = true;
+            }
+            h = (h ^ (uint64_t)(uint32_t)id) * kGolden;
+            h ^= h >> 29;
+        }
+    }
+    return (int64_t)(a.pow2 ? (h & a.rmask) : (h % a.R));
+}
+
+// Sequence s with offs[s] <= p < offs[s+1] (last such s; empty sequences skip).
+__device__ __forceinline__ int64_t find_seq(const int64_t *offs, int64_t n_seqs, int64_t p) {
+    int64_t lo = 0, hi = n_seqs;
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (__ldg(offs + mid) <= p) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Query q -> (sequence start, position); false if the position is invalid.
+__device__ __forceinline__ bool query_position(const HashParams &a, int64_t q, int64_t &start, int64_t &p) {
+    if (a.last_n == 0) {
+        p = __ldg(a.offs) + q;
+        const int64_t s = find_seq(a.offs, a.n_seqs, p);
+        start = __ldg(a.offs + s);
+        return p < __ldg(a.offs + s + 1);
+    }
+    const int64_t s = q / a.last_n;
+    const int64_t k = q - s * a.last_n;
+    start = __ldg(a.offs + s);
+    p = __ldg(a.offs + s + 1) - a.last_n + k;
+    return p >= start;
+}
+
+__global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashParams a, int64_t *__restrict__ idx) {
+    __shared__ uint64_t s_seed[kTables];
+    if (threadIdx.x < kTables) s_seed[threadIdx.x] = a.seeds[threadIdx.x];
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.last_n == 0 &&
+        __ldg(a.offs + a.n_seqs) - __ldg(a.offs) != a.n_query)
+        raise_error(ENGRAM_ERANGE);
+    __syncthreads();
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= a.n_query * kTables) return;
+    const int64_t q = g / kTables;
+    const int j = (int)(g - q * kTables);
+    int64_t start, p;
+    bool bad = false;
+    int64_t out = 0;
+    if (query_position(a, q, start, p)) {
+        out = hash_one(a, s_seed[j], j, start, p, bad);
+    } else {
+        bad = true;
+    }
+    if (bad) raise_error(ENGRAM_ERANGE);
+    idx[g] = out;
+}
+
+// ============================================================ gather-reduce ==
+// One warp per (query token, module).  Lane l reads 16 bytes of row
+// (2i + l/16) at byte offset 16*(l%16) for i = 0..11: each warp-wide load
+// covers two whole 256-byte rows and all 12 loads are issued before the
+// arithmetic, so a warp keeps 6 KB of random reads in flight.  The two
+// half-warps' partial sums are merged with one xor-16 shuffle.
+//
+// Row addresses come from an int64 idx array (HBM tables), an int32 slot
+// array (staged rows), or are hashed in-register by lanes 0..23 (the fused
+// path: no idx round trip).  The sums go out as fp32 mem or as bf16 X (the
+// projection's operand; bf16 rounding of the same fp32 sums, so both outputs
+// agree bit for bit after rounding).
+
+enum IdxMode { IDX_I64 = 0, IDX_STAGED_I32 = 1, IDX_HASH = 2 };
+
+struct GatherParams {
+    const uint8_t *rows;
+    const float *scales;
+    const void *idx;     // IDX_I64 / IDX_STAGED_I32
+    int64_t n_query;
+    int64_t R;           // rows per table (HBM) or staging capacity (staged)
+    void *out;           // float [n][512] or bf16 [n][512]
+    HashParams hp;       // IDX_HASH
+};
+
+template <int kMode, bool kBf16Out>
+__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams P) {
+    __shared__ uint64_t s_seed[kTables];
+    if (kMode == IDX_HASH) {
+        if (threadIdx.x < kTables) s_seed[threadIdx.x] = P.hp.seeds[threadIdx.x];
+        if (blockIdx.x == 0 && threadIdx.x == 0 && P.hp.last_n == 0 &&
+            __ldg(P.hp.offs + P.hp.n_seqs) - __ldg(P.hp.offs) != P.hp.n_query)
+            raise_error(ENGRAM_ERANGE);
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t t = gw >> 1;
+    const int m = (int)(gw & 1);
+    if (t >= P.n_query) return;
+
+    // lanes 0..23: this module's 24 row offsets and scales
+    int64_t off = 0;
+    float sc = 0.f;
+    int ok = 0;
+    if (lane < kTablesPerModule) {
+        const int j = kTablesPerModule * m + lane;
+        int64_t r;
+        if (kMode == IDX_HASH) {
+            int64_t start, p;
+            bool bad = !query_position(P.hp, t, start, p);
+            r = bad ? -1 : hash_one(P.hp, s_seed[j], j, start, p, bad);
+            if (bad) r = -1;
+        } else if (kMode == IDX_I64) {
+            r = __ldg(static_cast<const int64_t *>(P.idx) + t * kTables + j);
+        } else {
+            r = (int64_t)__ldg(static_cast<const int32_t *>(P.idx) + t * kTables + j);
+        }
+        ok = (r >= 0 && r < P.R);
+        if (!ok) raise_error(ENGRAM_ERANGE);
+        const int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
+        if (ok) {
+            off = flat * kRowBytes;
+            sc = __ldg(P.scales + flat);
+        }
+    }
+    const int half = lane >> 4;
+    const int c16 = lane & 15;
+    uint4 v[12];
+    float s[12];
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+        const int src = 2 * i + half;
+        const int64_t o = __shfl_sync(0xffffffffu, off, src);
+        const int k = __shfl_sync(0xffffffffu, ok, src);
+        s[i] = __shfl_sync(0xffffffffu, sc, src);
+        v[i] = k ? ld_nc_na_v4(P.rows + o + c16 * 16) : make_uint4(0, 0, 0, 0);
+    }
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 a = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
+            const float2 b = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
+            acc[4 * q + 0] = fmaf(s[i], a.x, acc[4 * q + 0]);
+            acc[4 * q + 1] = fmaf(s[i], a.y, acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(s[i], b.x, acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(s[i], b.y, acc[4 * q + 3]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
+    const int64_t col = t * kMem + 256 * m + 16 * c16 + 8 * half;
+    const float *a = acc + 8 * half;
+    if (kBf16Out) {
+        uint16_t *dst = static_cast<uint16_t *>(P.out) + col;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                                     pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+    } else {
+        float *dst = static_cast<float *>(P.out) + col;
+        reinterpret_cast<float4 *>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
+        reinterpret_cast<float4 *>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+    }
+}
+
+// ==================================================================== dedup ==
+// A bitmap over every (table, row) marks the rows the queries touch; an
+// exclusive prefix of per-word popcounts gives each distinct row a dense
+// slot, already sorted by (table, row); each query's index is then remapped
+// to its slot.  Three passes over the bitmap words: per-block popcount sums,
+// one-block scan of those sums, per-block word prefixes + the unique list.
+
+constexpr int kScanThreads = 256;
+constexpr int kScanWordsPerThread = 16;
+constexpr int kScanWordsPerBlock = kScanThreads * kScanWordsPerThread;
+
+__global__ void __launch_bounds__(256) dedup_mark_kernel(const int64_t *__restrict__ idx, int64_t n, int64_t R,
+                                                         int64_t W, uint32_t *__restrict__ bitmap) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n * kTables) return;
+    const int j = (int)(g % kTables);
+    const int64_t r = __ldg(idx + g);
+    if (r < 0 || r >= R) {
+        raise_error(ENGRAM_ERANGE);
+        return;
+    }
+    atomicOr(bitmap + (int64_t)j * W + (r >> 5), 1u << (r & 31));
+}
+
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t *total) {
+    __shared__ uint32_t warp_sums[kScanThreads / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        uint32_t ws = lane < kScanThreads / 32 ? warp_sums[lane] : 0u;
+        uint32_t wi = ws;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < kScanThreads / 32) warp_sums[lane] = wi - ws;
+        if (lane == kScanThreads / 32 - 1) *total = wi;
+    }
+    __syncthreads();
+    const uint32_t r = warp_sums[wid] + incl - x;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads) dedup_count_kernel(const uint32_t *__restrict__ bitmap,
+                                                                   int64_t n_words,
+                                                                   uint32_t *__restrict__ block_sums) {
+    const int64_t base = (int64_t)blockIdx.x * kScanWordsPerBlock + (int64_t)threadIdx.x * kScanWordsPerThread;
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 0; k < kScanWordsPerThread; ++k)
+        if (base + k < n_words) c += __popc(__ldg(bitmap + base + k));
+    __shared__ uint32_t total;
+    block_exclusive_scan(c, &total);
+    if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kScanThreads) dedup_scan_blocks_kernel(uint32_t *__restrict__ block_sums,
+                                                                         int64_t n_blocks, int64_t capacity,
+                                                                         int64_t *__restrict__ n_unique) {
+    __shared__ uint32_t total;
+    uint32_t carry = 0;
+    for (int64_t b0 = 0; b0 < n_blocks; b0 += kScanThreads) {
+        const int64_t b = b0 + threadIdx.x;
+        const uint32_t x = b < n_blocks ? block_sums[b] : 0u;
+        const uint32_t ex = block_exclusive_scan(x, &total);
+        if (b < n_blocks) block_sums[b] = carry + ex;
+        carry += total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        *n_unique = (int64_t)carry;
+        if ((int64_t)carry > capacity) raise_error(ENGRAM_ECAPACITY);
+    }
+}
+
+__global__ void __launch_bounds__(kScanThreads) dedup_emit_kernel(const uint32_t *__restrict__ bitmap,
+                                                                  int64_t n_words, int64_t W, int64_t R,
+                                                                  const uint32_t *__restrict__ block_offs,
+                                                                  uint32_t *__restrict__ word_prefix,
+                                                                  int64_t *__restrict__ unique,
+                                                                  int64_t capacity) {
+    const int64_t base = (int64_t)blockIdx.x * kScanWordsPerBlock + (int64_t)threadIdx.x * kScanWordsPerThread;
+    uint32_t wv[kScanWordsPerThread];
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 0; k < kScanWordsPerThread; ++k) {
+        wv[k] = base + k < n_words ? __ldg(bitmap + base + k) : 0u;
+        c += __popc(wv[k]);
+    }
+    __shared__ uint32_t total;
+    uint32_t pre = block_offs[blockIdx.x] + block_exclusive_scan(c, &total);
+#pragma unroll
+    for (int k = 0; k < kScanWordsPerThread; ++k) {
+        const int64_t w = base + k;
+        if (w >= n_words) break;
+        word_prefix[w] = pre;
+        uint32_t bits = wv[k];
+        const int64_t j = w / W;
+        const int64_t row0 = (w - j * W) * 32;
+        uint32_t slot = pre;
+        while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if ((int64_t)slot < capacity) unique[slot] = j * R + row0 + b;
+            ++slot;
+        }
+        pre += __popc(wv[k]);
+    }
+}
+
+__global__ void __launch_bounds__(256) dedup_remap_kernel(const int64_t *__restrict__ idx, int64_t n, int64_t R,
+                                                          int64_t W, const uint32_t *__restrict__ bitmap,
+                                                          const uint32_t *__restrict__ word_prefix,
+                                                          int64_t capacity, int32_t *__restrict__ idx_staged) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n * kTables) return;
+    const int j = (int)(g % kTables);
+    const int64_t r = __ldg(idx + g);
+    int32_t slot = 0;
+    if (r >= 0 && r < R) {
+        const int64_t w = (int64_t)j * W + (r >> 5);
+        const uint32_t below = __ldg(bitmap + w) & ((1u << (r & 31)) - 1u);
+        const int64_t s = (int64_t)__ldg(word_prefix + w) + __popc(below);
+        slot = s < capacity ? (int32_t)s : 0;
+    }
+    idx_staged[g] = slot;
+}
+
+// ==================================================================== stage ==
+// Copy unique rows (and their scales) from host tables into device staging.
+// Each half-warp moves one 256-byte row with 16-byte loads; a warp keeps four
+// row pairs in flight, and the grid strides over the unique list.
+
+__global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ host_tables,
+                                                    const float *__restrict__ host_scales,
+                                                    const int64_t *__restrict__ unique,
+                                                    const int64_t *__restrict__ n_unique, int64_t capacity,
+                                                    uint8_t *__restrict__ staged, float *__restrict__ staged_scales) {
+    const int64_t U = min(*n_unique, capacity);
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4, c16 = lane & 15;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    constexpr int kPairs = 4;
+    for (int64_t u0 = warp * 2 * kPairs; u0 < U; u0 += n_warps * 2 * kPairs) {
+        uint4 v[kPairs];
+        int64_t flat[kPairs];
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+            const int64_t u = u0 + 2 * k + half;
+            flat[k] = u < U ? __ldg(unique + u) : -1;
+            v[k] = flat[k] >= 0 ? *reinterpret_cast<const uint4 *>(host_tables + flat[k] * kRowBytes + c16 * 16)
+                                : make_uint4(0, 0, 0, 0);
+        }
+        float sc[kPairs];
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) sc[k] = (c16 == 0 && flat[k] >= 0) ? host_scales[flat[k]] : 0.f;
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+            const int64_t u = u0 + 2 * k + half;
+            if (flat[k] >= 0) {
+                *reinterpret_cast<uint4 *>(staged + u * kRowBytes + c16 * 16) = v[k];
+                if (c16 == 0) staged_scales[u] = sc[k];
+            }
+        }
+    }
+}
+
+// ================================================================ host side ==
+
+int num_sms() {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (sms[dev] == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev] = v > 0 ? v : 148;
+    }
+    return sms[dev];
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+engram_status check_config(const engram_config *cfg) {
+    if (!cfg) return ENGRAM_EINVAL;
+    if (cfg->vocab < 1 || cfg->rows < 1 || cfg->d_model < 0) return ENGRAM_EINVAL;
+    return ENGRAM_OK;
+}
+
+// With ENGRAM_DEBUG set in the environment, failed CUDA calls are reported on
+// stderr with the call site (the status returned is the same either way).
+static engram_status cuda_fail(cudaError_t e, const char *what) {
+    static const bool debug = getenv("ENGRAM_DEBUG") != nullptr;
+    if (debug) fprintf(stderr, "libengram: %s failed: %s\n", what, cudaGetErrorString(e));
+    return ENGRAM_ECUDA;
+}
+
+engram_status launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ENGRAM_OK : cuda_fail(e, "kernel launch");
+}
+
+static void fill_hash_params(HashParams &a, const engram_config *cfg, const int32_t *tokens, const int64_t *offs,
+                             int64_t n_seqs, int32_t last_n, int64_t n_query);
+
+engram_status hash_launch(const engram_config *cfg, const int32_t *tokens, const int64_t *offs, int64_t n_seqs,
+                          int32_t last_n, int64_t n_query, int64_t *idx, cudaStream_t st) {
+    HashParams a;
+    fill_hash_params(a, cfg, tokens, offs, n_seqs, last_n, n_query);
+    const int64_t threads = n_query * kTables;
+    const int64_t blocks = (threads + 255) / 256;
+    hash_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, idx);
+    return launch_status();
+}
+
+static void fill_hash_params(HashParams &a, const engram_config *cfg, const int32_t *tokens, const int64_t *offs,
+                             int64_t n_seqs, int32_t last_n, int64_t n_query) {
+    a.tokens = tokens;
+    a.offs = offs;
+    a.n_seqs = n_seqs;
+    a.n_query = n_query;
+    a.R = (uint64_t)cfg->rows;
+    a.pow2 = (cfg->rows & (cfg->rows - 1)) == 0;
+    a.rmask = (uint64_t)cfg->rows - 1;
+    a.V = cfg->vocab;
+    a.last_n = last_n;
+    memcpy(a.seeds, cfg->seeds, sizeof(a.seeds));
+}
+
+// mode: IDX_I64 / IDX_STAGED_I32 / IDX_HASH; out: fp32 mem or bf16 X.
+engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const float *scales, const void *idx,
+                            const HashParams *hp, int64_t n_query, int64_t R, void *out, cudaStream_t st) {
+    GatherParams P;
+    memset(&P, 0, sizeof(P));
+    P.rows = rows;
+    P.scales = scales;
+    P.idx = idx;
+    P.n_query = n_query;
+    P.R = R;
+    P.out = out;
+    if (hp) P.hp = *hp;
+    const int64_t warps = n_query * 2;
+    const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+#define ENGRAM_GATHER(M, B) gather_kernel<M, B><<<blocks, 256, 0, st>>>(P)
+    if (mode == IDX_I64) {
+        if (bf16_out) ENGRAM_GATHER(IDX_I64, true); else ENGRAM_GATHER(IDX_I64, false);
+    } else if (mode == IDX_STAGED_I32) {
+        if (bf16_out) ENGRAM_GATHER(IDX_STAGED_I32, true); else ENGRAM_GATHER(IDX_STAGED_I32, false);
+    } else {
+        if (bf16_out) ENGRAM_GATHER(IDX_HASH, true); else ENGRAM_GATHER(IDX_HASH, false);
+    }
+#undef ENGRAM_GATHER
+    return launch_status();
+}
+
+// dedup workspace: bitmap [48*W] u32 | word_prefix [48*W] u32 | block sums
+struct DedupLayout {
+    int64_t W, n_words, n_blocks;
+    size_t off_bitmap, off_prefix, off_blocks, total;
+};
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static DedupLayout dedup_layout(const engram_config *cfg) {
+    DedupLayout L;
+    L.W = (cfg->rows + 31) / 32;
+    L.n_words = L.W * kTables;
+    L.n_blocks = (L.n_words + kScanWordsPerBlock - 1) / kScanWordsPerBlock;
+    L.off_bitmap = 0;
+    L.off_prefix = round_up((size_t)L.n_words * 4, 256);
+    L.off_blocks = L.off_prefix + round_up((size_t)L.n_words * 4, 256);
+    L.total = L.off_blocks + round_up((size_t)L.n_blocks * 4, 256);
+    return L;
+}
+
+size_t dedup_bytes(const engram_config *cfg) { return dedup_layout(cfg).total; }
+
+engram_status dedup_launch(const engram_config *cfg, const int64_t *idx, int64_t n_query, void *ws,
+                           int64_t *unique, int64_t capacity, int32_t *idx_staged, int64_t *n_unique,
+                           cudaStream_t st) {
+    const DedupLayout L = dedup_layout(cfg);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(base + L.off_bitmap);
+    uint32_t *prefix = reinterpret_cast<uint32_t *>(base + L.off_prefix);
+    uint32_t *blocks = reinterpret_cast<uint32_t *>(base + L.off_blocks);
+    if (cudaMemsetAsync(bitmap, 0, (size_t)L.n_words * 4, st) != cudaSuccess) return ENGRAM_ECUDA;
+    const int64_t n = n_query * kTables;
+    const unsigned gb = (unsigned)((n + 255) / 256);
+    if (n > 0) dedup_mark_kernel<<<gb, 256, 0, st>>>(idx, n_query, cfg->rows, L.W, bitmap);
+    dedup_count_kernel<<<(unsigned)L.n_blocks, kScanThreads, 0, st>>>(bitmap, L.n_words, blocks);
+    dedup_scan_blocks_kernel<<<1, kScanThreads, 0, st>>>(blocks, L.n_blocks, capacity, n_unique);
+    dedup_emit_kernel<<<(unsigned)L.n_blocks, kScanThreads, 0, st>>>(bitmap, L.n_words, L.W, cfg->rows, blocks,
+                                                                      prefix, unique, capacity);
+    if (n > 0)
+        dedup_remap_kernel<<<gb, 256, 0, st>>>(idx, n_query, cfg->rows, L.W, bitmap, prefix, capacity,
+                                               idx_staged);
+    return launch_status();
+}
+
+engram_status stage_launch(const uint8_t *host_tables, const float *host_scales, const int64_t *unique,
+                           const int64_t *n_unique, int64_t capacity, uint8_t *staged, float *staged_scales,
+                           cudaStream_t st) {
+    const int blocks = num_sms() * 8;
+    stage_kernel<<<blocks, 256, 0, st>>>(host_tables, host_scales, unique, n_unique, capacity, staged,
+                                         staged_scales);
+    return launch_status();
+}
+
+
+// ----------------------------------------------------------- fuse launcher --
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] (inner contiguous), box [box_outer][box_inner],
+// 128-byte swizzle: a box row of 64 bf16 is one swizzle span.
+static bool bf16_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                        uint32_t box_outer) {
+    auto enc = tensormap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// CTAs per cluster (d slices) for a projection of m_tiles tiles and n_chunks
+// 256-column chunks: few tiles spread d over up to 8 CTAs; many tiles use
+// slices of at most 4 chunks so each CTA's h slice stays small in L2.
+static int pick_groups(int64_t m_tiles, int n_chunks) {
+    int g = 1;
+    const int sms = num_sms();
+    if (m_tiles * 2 < sms) {
+        while (g * 2 <= fuse::MAX_GROUPS && n_chunks % (g * 2) == 0 && m_tiles * g * 2 <= sms) g *= 2;
+    } else {
+        while (n_chunks / g > 4 && g * 2 <= fuse::MAX_GROUPS && n_chunks % (g * 2) == 0) g *= 2;
+    }
+    while (n_chunks / g > 16 && g * 2 <= fuse::MAX_GROUPS && n_chunks % (g * 2) == 0) g *= 2;
+    return g;
+}
+
+template <int XSRC>
+static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
+                                   cudaStream_t st) {
+    auto kern = fuse::fuse_kernel<XSRC>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fuse::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fuse smem)");
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.groups;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(fuse::NUM_THREADS);
+    cfg.dynamicSmemBytes = fuse::SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent: as many clusters as fit at once, each striding over tiles
+    static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
+    int &mc = max_clusters[dev][p.groups];
+    if (mc == 0) {
+        cfg.gridDim = dim3(p.groups * 64);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms() / p.groups;
+        }
+        mc = n;
+    }
+    const int64_t clusters = std::min<int64_t>(p.m_tiles, mc);
+    cfg.gridDim = dim3((unsigned)(clusters * p.groups));
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, wmap, xmap, p);
+    if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(fuse)");
+    return launch_status();
+}
+
+// y = X @ W_out and the gated residual update.  X comes either from fp32 mem
+// (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
+engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint16_t *x_bf16, const uint16_t *W,
+                          const uint16_t *g, uint16_t *h, int64_t n_query, cudaStream_t st) {
+    const int d = cfg->d_model;
+    const int n_chunks = d / fuse::BN;
+    fuse::Params p;
+    p.mem = mem;
+    p.g = g;
+    p.h = h;
+    p.n_query = n_query;
+    p.m_tiles = (n_query + fuse::BM - 1) / fuse::BM;
+    p.d = d;
+    p.groups = pick_groups(p.m_tiles, n_chunks);
+    p.cpg = n_chunks / p.groups;
+    p.eps = cfg->rms_eps;
+    p.inv_sqrt_d = 1.0f / sqrtf((float)d);
+    if (p.cpg > 16) return ENGRAM_EINVAL;
+    CUtensorMap wmap, xmap;
+    memset(&xmap, 0, sizeof(xmap));
+    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, fuse::BK)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
+    if (x_bf16) {
+        if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
+            return cuda_fail(cudaErrorInvalidValue, "X tensor map");
+        return fuse_launch_t<fuse::X_FROM_BF16_TMA>(wmap, xmap, p, st);
+    }
+    return fuse_launch_t<fuse::X_FROM_F32_MEM>(wmap, xmap, p, st);
+}
+
+engram_status check_fuse_args(const engram_config *cfg, const void *W, const void *g, const void *h) {
+    const int d = cfg->d_model;
+    if (d < fuse::BN || d % fuse::BN != 0 || d > 16 * fuse::BN * fuse::MAX_GROUPS) return ENGRAM_EINVAL;
+    if (!W || !g || !h) return ENGRAM_EINVAL;
+    if (!aligned(W, 16) || !aligned(g, 16) || !aligned(h, 16)) return ENGRAM_EINVAL;
+    if (!(cfg->rms_eps >= 0.0f)) return ENGRAM_EINVAL;
+    return ENGRAM_OK;
+}
+
+// forward workspace: X [n][512] bf16
+static size_t forward_bytes(int64_t n) { return round_up((size_t)n * kMem * 2, 256); }
+
+}  // namespace engram
+
+using namespace engram;
+
+// ================================================================= C ABI ====
+
+extern "C" const char *engram_status_string(engram_status st) {
+    switch (st) {
+        case ENGRAM_OK: return "ok";
+        case ENGRAM_EINVAL: return "invalid argument";
+        case ENGRAM_ECUDA: return "CUDA error";
+        case ENGRAM_ERANGE: return "value out of range (token id, position or row index)";
+        case ENGRAM_ECAPACITY: return "more unique rows than the staging capacity";
+        case ENGRAM_ETIMEOUT: return "a bounded device-side wait timed out";
+        case ENGRAM_ENOMEM: return "workspace too small";
+        case ENGRAM_EUNSUPPORTED: return "unsupported device or feature";
+    }
+    return "unknown status";
+}
+
+extern "C" engram_status engram_last_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ENGRAM_ECUDA;
+    unsigned int w = 0;
+    if (cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w)) != cudaSuccess) return ENGRAM_ECUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return ENGRAM_ECUDA;
+    for (int k = 1; k < 32; ++k)
+        if (w & (1u << k)) return (engram_status)k;
+    return ENGRAM_OK;
+}
+
+extern "C" engram_status engram_hash(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                                     int64_t n_seqs, int32_t last_n, int64_t n_query, int64_t *idx, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || !idx || n_seqs < 1) return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (!aligned(idx, 8) || !aligned(seq_offsets, 8) || !aligned(tokens, 4)) return ENGRAM_EINVAL;
+    if (n_query > (INT64_C(1) << 40)) return ENGRAM_EINVAL;
+    return hash_launch(cfg, tokens, seq_offsets, n_seqs, last_n, n_query, idx, (cudaStream_t)stream);
+}
+
+extern "C" engram_status engram_gather_reduce(const engram_config *cfg, const uint8_t *tables, const float *scales,
+                                              const int64_t *idx, int64_t n_query, float *mem, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tables || !scales || !idx || !mem) return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(idx, 8) || !aligned(mem, 16)) return ENGRAM_EINVAL;
+    return gather_launch(IDX_I64, false, tables, scales, idx, nullptr, n_query, cfg->rows, mem, (cudaStream_t)stream);
+}
+
+extern "C" size_t engram_dedup_workspace_bytes(const engram_config *cfg) {
+    if (check_config(cfg) != ENGRAM_OK) return 0;
+    return dedup_bytes(cfg);
+}
+
+extern "C" engram_status engram_dedup(const engram_config *cfg, const int64_t *idx, int64_t n_query, void *workspace,
+                                      size_t workspace_bytes, int64_t *unique, int64_t capacity,
+                                      int32_t *idx_staged, int64_t *n_unique, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || capacity < 1) return ENGRAM_EINVAL;
+    if (!workspace || !unique || !n_unique || (n_query > 0 && (!idx || !idx_staged))) return ENGRAM_EINVAL;
+    if (n_query * kTables >= (INT64_C(1) << 31) || capacity >= (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    if (!aligned(workspace, 256) || !aligned(unique, 8) || !aligned(n_unique, 8)) return ENGRAM_EINVAL;
+    if (workspace_bytes < dedup_bytes(cfg)) return ENGRAM_ENOMEM;
+    return dedup_launch(cfg, idx, n_query, workspace, unique, capacity, idx_staged, n_unique, (cudaStream_t)stream);
+}
+
+extern "C" engram_status engram_stage(const engram_config *cfg, const uint8_t *host_tables, const float *host_scales,
+                                      const int64_t *unique, const int64_t *n_unique, int64_t capacity,
+                                      uint8_t *staged_rows, float *staged_scales, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || capacity < 1) return ENGRAM_EINVAL;
+    if (!host_tables || !host_scales || !unique || !n_unique || !staged_rows || !staged_scales) return ENGRAM_EINVAL;
+    if (!aligned(host_tables, 16) || !aligned(staged_rows, 16) || !aligned(host_scales, 4)) return ENGRAM_EINVAL;
+    return stage_launch(host_tables, host_scales, unique, n_unique, capacity, staged_rows, staged_scales,
+                        (cudaStream_t)stream);
+}
+
+extern "C" engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_t *staged_rows,
+                                                     const float *staged_scales, const int32_t *idx_staged,
+                                                     int64_t n_query, int64_t capacity, float *mem, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || capacity < 1) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!staged_rows || !staged_scales || !idx_staged || !mem) return ENGRAM_EINVAL;
+    if (!aligned(staged_rows, 16) || !aligned(mem, 16) || !aligned(idx_staged, 4)) return ENGRAM_EINVAL;
+    return gather_launch(IDX_STAGED_I32, false, staged_rows, staged_scales, idx_staged, nullptr, n_query, capacity, mem,
+                         (cudaStream_t)stream);
+}
+
+extern "C" engram_status engram_fuse(const engram_config *cfg, const float *mem, const uint16_t *W_out,
+                                     const uint16_t *g, uint16_t *h, int64_t n_query, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK || !mem || !aligned(mem, 16)) return ENGRAM_EINVAL;
+    if (n_query > (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    return fuse_launch(cfg, mem, nullptr, W_out, g, h, n_query, (cudaStream_t)stream);
+}
+
+extern "C" size_t engram_forward_workspace_bytes(const engram_config *cfg, int64_t n_query) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0) return 0;
+    return forward_bytes(n_query);
+}
+
+extern "C" engram_status engram_forward(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                                        int64_t n_seqs, int32_t last_n, int64_t n_query, const uint8_t *tables,
+                                        const float *scales, const uint16_t *W_out, const uint16_t *g, uint16_t *h,
+                                        void *workspace, size_t workspace_bytes, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales || !workspace) return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(workspace, 256) || !aligned(tokens, 4) ||
+        !aligned(seq_offsets, 8))
+        return ENGRAM_EINVAL;
+    if (n_query > (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    if (workspace_bytes < forward_bytes(n_query)) return ENGRAM_ENOMEM;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint16_t *X = static_cast<uint16_t *>(workspace);
+    HashParams hp;
+    fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
+    engram_status s = gather_launch(IDX_HASH, true, tables, scales, nullptr, &hp, n_query, cfg->rows, X, st);
+    if (s != ENGRAM_OK) return s;
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
+}
+
+extern "C" engram_status engram_gather_x(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                                         int64_t n_seqs, int32_t last_n, int64_t n_query, const uint8_t *tables,
+                                         const float *scales, uint16_t *X, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales || !X) return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(X, 16) || !aligned(tokens, 4) ||
+        !aligned(seq_offsets, 8))
+        return ENGRAM_EINVAL;
+    if (n_query > (INT64_C(1) << 40)) return ENGRAM_EINVAL;
+    HashParams hp;
+    fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
+    return gather_launch(IDX_HASH, true, tables, scales, nullptr, &hp, n_query, cfg->rows, X, (cudaStream_t)stream);
+}
+
+extern "C" engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const uint16_t *W_out,
+                                       const uint16_t *g, uint16_t *h, int64_t n_query, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK || !X || !aligned(X, 16)) return ENGRAM_EINVAL;
+    if (n_query > (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, (cudaStream_t)stream);
+}
+
+extern "C" size_t engram_forward_host_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t capacity) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || capacity < 1) return 0;
+    return round_up((size_t)n_query * kTables * 8, 256)      // idx
+           + round_up((size_t)n_query * kTables * 4, 256)    // idx_staged
+           + round_up((size_t)n_query * kMem * 2, 256)       // X (bf16)
+           + round_up((size_t)capacity * 8, 256)             // unique
+           + round_up((size_t)capacity * kRowBytes, 256)     // staged rows
+           + round_up((size_t)capacity * 4, 256)             // staged scales
+           + dedup_bytes(cfg);
+}
+
+extern "C" engram_status engram_forward_host(const engram_config *cfg, const int32_t *tokens,
+                                             const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                             int64_t n_query, const uint8_t *host_tables, const float *host_scales,
+                                             const uint16_t *W_out, const uint16_t *g, uint16_t *h, int64_t capacity,
+                                             void *workspace, size_t workspace_bytes, int64_t *n_unique, void *stream,
+                                             void *side_stream, void *ev_dedup, void *ev_staged) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0 || capacity < 1)
+        return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !host_tables || !host_scales || !workspace || !n_unique ||
+        !ev_dedup || !ev_staged)
+        return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
+    if (!aligned(host_tables, 16) || !aligned(host_scales, 4) || !aligned(workspace, 256) || !aligned(n_unique, 8))
+        return ENGRAM_EINVAL;
+    if (n_query * kTables >= (INT64_C(1) << 31) || capacity >= (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    if (workspace_bytes < engram_forward_host_workspace_bytes(cfg, n_query, capacity)) return ENGRAM_ENOMEM;
+    cudaStream_t st = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    size_t o = 0;
+    int64_t *idx = reinterpret_cast<int64_t *>(ws + o);
+    o += round_up((size_t)n_query * kTables * 8, 256);
+    int32_t *idx_staged = reinterpret_cast<int32_t *>(ws + o);
+    o += round_up((size_t)n_query * kTables * 4, 256);
+    uint16_t *X = reinterpret_cast<uint16_t *>(ws + o);
+    o += round_up((size_t)n_query * kMem * 2, 256);
+    int64_t *unique = reinterpret_cast<int64_t *>(ws + o);
+    o += round_up((size_t)capacity * 8, 256);
+    uint8_t *rows = ws + o;
+    o += round_up((size_t)capacity * kRowBytes, 256);
+    float *sc = reinterpret_cast<float *>(ws + o);
+    o += round_up((size_t)capacity * 4, 256);
+    void *dws = ws + o;
+    engram_status s = hash_launch(cfg, tokens, seq_offsets, n_seqs, last_n, n_query, idx, st);
+    if (s != ENGRAM_OK) return s;
+    s = dedup_launch(cfg, idx, n_query, dws, unique, capacity, idx_staged, n_unique, st);
+    if (s != ENGRAM_OK) return s;
+    if (cudaEventRecord((cudaEvent_t)ev_dedup, st) != cudaSuccess) return ENGRAM_ECUDA;
+    if (cudaStreamWaitEvent(side, (cudaEvent_t)ev_dedup, 0) != cudaSuccess) return ENGRAM_ECUDA;
+    s = stage_launch(host_tables, host_scales, unique, n_unique, capacity, rows, sc, side);
+    if (s != ENGRAM_OK) return s;
+    if (cudaEventRecord((cudaEvent_t)ev_staged, side) != cudaSuccess) return ENGRAM_ECUDA;
+    if (cudaStreamWaitEvent(st, (cudaEvent_t)ev_staged, 0) != cudaSuccess) return ENGRAM_ECUDA;
+    s = gather_launch(IDX_STAGED_I32, true, rows, sc, idx_staged, nullptr, n_query, capacity, X, st);
+    if (s != ENGRAM_OK) return s;
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
+}

@@ -1,0 +1,376 @@
+// The gated projection into the residual stream on tcgen05 tensor cores.
+//
+// Work split: a tile is 128 query tokens; a thread-block cluster of G CTAs
+// shares a tile and splits d into G slices of d/G columns.  Every CTA holds
+// the whole X = bf16(mem) tile [128 x 512] in shared memory (K-major,
+// 128-byte swizzle), streams its W_out slice through a 3-stage TMA ring in
+// [64 K-rows x 256 N] pieces (MN-major, 128-byte swizzle), and accumulates
+// y = X @ W_out in fp32 in TMEM with tcgen05.mma (M=128, N=256, K=16),
+// double-buffered over 256-column chunks so the epilogue of one chunk
+// overlaps the MMAs of the next.
+//
+// The gate of a token needs its whole h row, but each CTA only owns d/G
+// columns: each CTA reduces sum(h^2) and <h,g> over its slice, the partial
+// sums are exchanged through distributed shared memory (remote mbarrier
+// arrivals, cluster-scope acquire), and every CTA adds the G partials in the
+// same order, so all CTAs hold bit-identical gates before any CTA writes h.
+// The epilogue thread that owns a TMEM lane owns that token: it re-reads its
+// slice of h (an L2 hit: the slice was just read for the gate) and writes
+// h = bf16(h + gate * y).
+//
+// Sources: rohitghumare.com "guides/deepseek-v4-1-flash", sections "The
+// architecture" (Engram rows are added into the residual stream through a
+// learned gate) and "Engram: the table that is never multiplied".
+#pragma once
+
+namespace engram {
+namespace fuse {
+
+constexpr int BM = 128;                            // tokens per tile (TMEM lanes)
+constexpr int BN = 256;                            // d columns per chunk (MMA N)
+constexpr int BK = 64;                             // K rows per W stage
+constexpr int KSTAGES = kMem / BK;                 // 8 W stages per chunk
+constexpr int NSTAGE = 3;                          // W ring depth
+constexpr int X_KBLOCK_BYTES = BM * BK * 2;        // 16 KB: 128 rows x 128 B
+constexpr int X_BYTES = X_KBLOCK_BYTES * KSTAGES;  // 128 KB
+constexpr int W_BOX_BYTES = BK * 64 * 2;           // 8 KB: 64 K-rows x 64 N
+constexpr int W_STAGE_BYTES = W_BOX_BYTES * (BN / 64);  // 32 KB
+constexpr int TMEM_COLS = 2 * BN;                  // two accumulators
+constexpr int NUM_THREADS = 192;                   // warp0 TMA, warp1 MMA, warps2-5 epilogue
+constexpr int MAX_GROUPS = 8;                      // portable cluster size
+constexpr uint32_t IDESC = idesc_bf16(BM, BN, /*b_mn_major=*/true);
+
+enum XSource { X_FROM_F32_MEM = 0, X_FROM_BF16_TMA = 1 };
+
+struct Shared {
+    uint64_t full[NSTAGE];
+    uint64_t empty[NSTAGE];
+    uint64_t x_full;
+    uint64_t x_empty;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t gate_bar[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    float2 part[2][BM];  // (sum h^2, <h,g>) over this CTA's slice, per token
+};
+
+// 128 KB X + 96 KB W ring + barriers/partials = 231,552 B of the 232,448 B a
+// CTA may use; the dynamic buffer is declared 1024-byte aligned (swizzle atoms).
+constexpr int SMEM_BYTES = X_BYTES + NSTAGE * W_STAGE_BYTES + (int)sizeof(Shared);
+static_assert(SMEM_BYTES <= 232448, "fuse kernel shared memory over the per-CTA limit");
+
+struct Params {
+    const float *mem;  // [n_query][512] fp32 (X_FROM_F32_MEM)
+    const uint16_t *g; // [d] bf16
+    uint16_t *h;       // [n_query][d] bf16, in place
+    int64_t n_query;
+    int64_t m_tiles;
+    int32_t d;
+    int32_t groups;    // CTAs per cluster = d slices
+    int32_t cpg;       // 256-column chunks per CTA
+    float eps;
+    float inv_sqrt_d;
+};
+
+template <int XSRC>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fuse_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
+                const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if ((smem_u32(smem) & 1023u) != 0) {  // same for every CTA: all leave together
+        if (threadIdx.x == 0) raise_error(ENGRAM_EUNSUPPORTED);
+        return;
+    }
+    uint8_t *x_smem = smem;
+    uint8_t *w_smem = smem + X_BYTES;
+    Shared *sh = reinterpret_cast<Shared *>(smem + X_BYTES + NSTAGE * W_STAGE_BYTES);
+    volatile int *abort = &sh->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cl = cluster_id_x();
+    const int64_t n_cl = nclusters_x();
+    const int c0 = (int)rank * p.cpg;  // first chunk of this CTA's d slice
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&sh->full[s], 1);
+            mbar_init(&sh->empty[s], 1);
+        }
+        mbar_init(&sh->x_full, XSRC == X_FROM_F32_MEM ? 4 : 1);
+        mbar_init(&sh->x_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh->acc_full[b], 1);
+            mbar_init(&sh->acc_empty[b], 4);
+            mbar_init(&sh->gate_bar[b], 4 * p.groups);
+        }
+        mbar_init(&sh->done, 1);
+        sh->abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&w_map);
+        if (XSRC == X_FROM_BF16_TMA) prefetch_tensormap(&x_map);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // barriers of every CTA initialised before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem_base = sh->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool issued[NSTAGE] = {};
+            uint32_t issued_parity[NSTAGE] = {};
+            bool x_issued = false;
+            uint32_t x_it = 0;
+            for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl, ++x_it) {
+                if (XSRC == X_FROM_BF16_TMA) {
+                    if (!mbar_wait(&sh->x_empty, (x_it & 1u) ^ 1u, abort)) break;
+                    mbar_arrive_expect_tx(&sh->x_full, X_BYTES);
+                    for (int kb = 0; kb < KSTAGES; ++kb)
+                        tma_load_2d(x_smem + kb * X_KBLOCK_BYTES, &x_map, &sh->x_full, kb * BK, (int)(mt * BM));
+                    x_issued = true;
+                }
+                for (int c = c0; c < c0 + p.cpg && !*abort; ++c) {
+                    for (int ks = 0; ks < KSTAGES; ++ks) {
+                        if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort)) break;
+                        mbar_arrive_expect_tx(&sh->full[stage], W_STAGE_BYTES);
+                        uint8_t *dst = w_smem + stage * W_STAGE_BYTES;
+#pragma unroll
+                        for (int b = 0; b < BN / 64; ++b)
+                            tma_load_2d(dst + b * W_BOX_BYTES, &w_map, &sh->full[stage], c * BN + b * 64, ks * BK);
+                        issued[stage] = true;
+                        issued_parity[stage] = phase;
+                        if (++stage == NSTAGE) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            // Never leave the CTA with a copy still landing in its shared memory.
+            int no_abort = 0;
+            for (int s = 0; s < NSTAGE; ++s)
+                if (issued[s]) mbar_wait(&sh->full[s], issued_parity[s], &no_abort, 200000000ull);
+            if (x_issued) mbar_wait(&sh->x_full, (x_it - 1u) & 1u, &no_abort, 200000000ull);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t x_phase = 0;
+            uint32_t acc_it = 0;
+            const uint32_t x_addr = smem_u32(x_smem);
+            const uint32_t w_addr = smem_u32(w_smem);
+            bool ok = true;
+            for (int64_t mt = cl; mt < p.m_tiles && ok && !*abort; mt += n_cl) {
+                if (!mbar_wait(&sh->x_full, x_phase, abort)) break;
+                x_phase ^= 1u;
+                tc_fence_after();
+                for (int c = 0; c < p.cpg && ok; ++c, ++acc_it) {
+                    const uint32_t buf = acc_it & 1u;
+                    const uint32_t use = acc_it >> 1;
+                    if (!mbar_wait(&sh->acc_empty[buf], (use & 1u) ^ 1u, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    for (int ks = 0; ks < KSTAGES; ++ks) {
+                        if (!mbar_wait(&sh->full[stage], phase, abort)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int s = 0; s < BK / 16; ++s) {
+                            // A: K-block ks, K-step s = 32 bytes into each 128-byte swizzled row
+                            const uint64_t adesc =
+                                smem_desc(x_addr + ks * X_KBLOCK_BYTES + s * 32, 16, 1024, kSwizzle128B);
+                            // B: 16 K-rows (2 x 8-row groups of 1 KB) further; N atoms of 64 are 8 KB apart
+                            const uint64_t bdesc =
+                                smem_desc(w_addr + stage * W_STAGE_BYTES + s * 2048, W_BOX_BYTES, 1024, kSwizzle128B);
+                            mma_bf16(d_tmem, adesc, bdesc, IDESC, (ks | s) != 0);
+                        }
+                        mma_commit(&sh->empty[stage]);
+                        if (++stage == NSTAGE) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok) mma_commit(&sh->acc_full[buf]);
+                }
+                if (ok) mma_commit(&sh->x_empty);
+            }
+            // All MMAs issued by this thread complete before TMEM is released.
+            mma_commit(&sh->done);
+            int no_abort = 0;
+            mbar_wait(&sh->done, 0, &no_abort, 200000000ull);
+        }
+    } else {
+        // ------------------------------------------------------ epilogue ----
+        const int q = warp & 3;         // TMEM lane quadrant of this warp
+        const int ew = warp - 2;        // 0..3
+        const int row = q * 32 + lane;  // token row within the tile owned by this thread
+        const int slice_cols = p.cpg * BN;
+        const int64_t col0 = (int64_t)c0 * BN;
+        uint32_t it = 0;
+        uint32_t acc_it = 0;
+        for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl, ++it) {
+            const int64_t m0 = mt * BM;
+
+            if (XSRC == X_FROM_F32_MEM) {
+                // X = bf16(mem): row r, K-block kb, 16-byte chunk c at
+                // kb*16K + r*128 + ((c ^ (r & 7)) * 16)   (128-byte swizzle)
+                if (!mbar_wait(&sh->x_empty, (it & 1u) ^ 1u, abort)) break;
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = ew * 32 + rr;
+                    const int64_t t = m0 + r;
+#pragma unroll
+                    for (int k4 = 0; k4 < kMem / 128; ++k4) {
+                        const int col = k4 * 128 + lane * 4;
+                        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (t < p.n_query) f = __ldg(reinterpret_cast<const float4 *>(p.mem + t * kMem + col));
+                        const uint32_t lo = pack_bf16x2(f.x, f.y), hi = pack_bf16x2(f.z, f.w);
+                        const int kb = col >> 6;
+                        const int byte = (col & 63) * 2;
+                        uint8_t *dst =
+                            x_smem + kb * X_KBLOCK_BYTES + r * 128 + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15);
+                        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(dst)), "r"(lo), "r"(hi)
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh->x_full);
+            }
+
+            // Partial gate sums over this CTA's slice for the warp's 32 tokens.
+            // Lanes stride over the slice's 16-byte pieces (coalesced); several
+            // rows are loaded before they are reduced to keep reads in flight.
+            const int per_lane = slice_cols / 8 / 32;  // 16-byte pieces per lane per row (= cpg <= 16)
+            const int rows_per_batch = 16 / per_lane;
+            float2 mine = make_float2(0.f, 0.f);
+            for (int rb = 0; rb < 32; rb += rows_per_batch) {
+                float ss[16], dt[16];
+                uint4 hv[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int rr = rb + k / per_lane;
+                    const int pc = lane + 32 * (k % per_lane);
+                    const int64_t t = m0 + q * 32 + rr;
+                    hv[k] = make_uint4(0, 0, 0, 0);
+                    if (k < rows_per_batch * per_lane && rr < 32 && t < p.n_query) {
+                        hv[k] = *reinterpret_cast<const uint4 *>(p.h + t * p.d + col0 + (int64_t)pc * 8);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int pc = lane + 32 * (k % per_lane);
+                    const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(p.g + col0) + pc);
+                    const uint32_t hw[4] = {hv[k].x, hv[k].y, hv[k].z, hv[k].w};
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                    float s2 = 0.f, d2 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = bf16_lo(hw[e]), a1 = bf16_hi(hw[e]);
+                        s2 = fmaf(a0, a0, s2);
+                        s2 = fmaf(a1, a1, s2);
+                        d2 = fmaf(a0, bf16_lo(gw[e]), d2);
+                        d2 = fmaf(a1, bf16_hi(gw[e]), d2);
+                    }
+                    ss[k] = s2;
+                    dt[k] = d2;
+                }
+                for (int rr = 0; rr < rows_per_batch && rb + rr < 32; ++rr) {
+                    float s = 0.f, d = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (k / per_lane == rr) {
+                            s += ss[k];
+                            d += dt[k];
+                        }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        s += __shfl_xor_sync(0xffffffffu, s, o);
+                        d += __shfl_xor_sync(0xffffffffu, d, o);
+                    }
+                    if (lane == rb + rr) mine = make_float2(s, d);
+                }
+            }
+            const uint32_t pb = it & 1u;
+            sh->part[pb][row] = mine;
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t bar = smem_u32(&sh->gate_bar[pb]);
+                for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+            }
+            if (!mbar_wait_cluster(&sh->gate_bar[pb], (it >> 1) & 1u, abort)) break;
+            float ssum = 0.f, dsum = 0.f;
+            const uint32_t my_part = smem_u32(&sh->part[pb][row]);
+            for (int r = 0; r < p.groups; ++r) {  // same order in every CTA
+                const float2 v = ld_shared_cluster_f2(mapa_shared(my_part, (uint32_t)r));
+                ssum += v.x;
+                dsum += v.y;
+            }
+            const float rinv = rsqrtf(ssum / (float)p.d + p.eps);
+            const float gate = 1.f / (1.f + __expf(-(rinv * dsum * p.inv_sqrt_d)));
+
+            // Epilogue per chunk: h = bf16(h + gate * y), 64 columns per step.
+            const int64_t t = m0 + row;
+            const bool live = t < p.n_query;
+            bool ok = true;
+            for (int c = 0; c < p.cpg; ++c, ++acc_it) {
+                const uint32_t buf = acc_it & 1u;
+                const uint32_t use = acc_it >> 1;
+                if (!mbar_wait(&sh->acc_full[buf], use & 1u, abort)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int g64 = 0; g64 < BN / 64; ++g64) {
+                    uint4 *hp = reinterpret_cast<uint4 *>(p.h + t * p.d + col0 + (int64_t)c * BN + g64 * 64);
+                    uint4 hv[8];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) hv[v] = live ? hp[v] : make_uint4(0, 0, 0, 0);
+                    uint32_t y[2][32];
+                    const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + g64 * 64;
+                    tmem_ld_32x32b_x32(ta, y[0]);
+                    tmem_ld_32x32b_x32(ta + 32, y[1]);
+                    tmem_ld_wait();
+                    if (live) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            uint32_t w[4] = {hv[v].x, hv[v].y, hv[v].z, hv[v].w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float y0 = __uint_as_float(y[v >> 2][(v & 3) * 8 + 2 * k]);
+                                const float y1 = __uint_as_float(y[v >> 2][(v & 3) * 8 + 2 * k + 1]);
+                                w[k] = pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])));
+                            }
+                            hp[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
+            }
+            if (!ok) break;
+        }
+    }
+
+    // No CTA leaves while a peer may still read its partial sums, and TMEM is
+    // released only after every MMA and TMEM load of this CTA is done.
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace fuse
+}  // namespace engram

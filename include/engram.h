@@ -1,0 +1,210 @@
+/*
+ * engram.h -- C ABI of libengram.so: the Engram memory read of
+ * DeepSeek-V4.1-Flash on one GB300 (sm_103a).
+ *
+ * What it computes, per query token t (sources: vramglass.com
+ * "deepseek-v4-1-flash-local-deployment", section "What makes up the 511 GB
+ * of weights?"; rohitghumare.com "guides/deepseek-v4-1-flash", sections
+ * "Engram: the table that is never multiplied" and "The architecture"):
+ *   1. the suffix 2-, 3- and 4-grams of token ids ending at t (positions
+ *      before the start of t's sequence read the pad id V);
+ *   2. 2 modules x 3 orders x 8 heads = 48 hashes, table j =
+ *      (module*3 + order-2)*8 + head; for each, h = seed[j], then for every
+ *      id of the n-gram, oldest first: h = (h ^ id) * 0x9E3779B97F4A7C15
+ *      (mod 2^64); h ^= h >> 29; and idx[t][j] = h mod R;
+ *   3. mem[t][256*m + c] = sum over module m's 24 tables of
+ *      scale[j][idx] * e4m3(table[j][idx][c])   (fp32 sums);
+ *   4. X = bf16(mem) [T,512]; y = X @ W_out [512,d] (fp32 accumulation);
+ *   5. h[t] += sigmoid(<h[t]/rms(h[t]), g> / sqrt(d)) * y[t], rounded to bf16,
+ *      rms(v) = sqrt(mean(v^2) + eps).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless a parameter says "host".  Pinned
+ *     host memory that the device can address (cudaHostAlloc, or memory the
+ *     GPU reaches over NVLink-C2C) is accepted where it says "host tables".
+ *   - The caller owns every buffer, stream and event; the library allocates
+ *     no memory.  Workspaces are sized by the matching *_workspace_bytes().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on its stream(s) and returns;
+ *     no call synchronises with the host except engram_last_error().
+ *   - Arguments are validated before anything is enqueued; a bad argument
+ *     returns ENGRAM_EINVAL and enqueues nothing.  A failed launch returns
+ *     ENGRAM_ECUDA.  Conditions only the device can see (token ids out of
+ *     range, a sequence shorter than last_n, an index >= R, more unique rows
+ *     than the staging capacity, a pipeline wait that ran out of time) set a
+ *     sticky per-device error word that engram_last_error() returns; the
+ *     kernels never trap.
+ *   - n_query == 0 is a no-op that returns ENGRAM_OK.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ENGRAM_OK = 0,
+    ENGRAM_EINVAL = 1,      /* bad argument (null, misaligned, size) */
+    ENGRAM_ECUDA = 2,       /* a CUDA call or launch failed */
+    ENGRAM_ERANGE = 3,      /* device saw a token id, position or index out of range */
+    ENGRAM_ECAPACITY = 4,   /* more unique rows than the staging capacity */
+    ENGRAM_ETIMEOUT = 5,    /* a bounded device-side wait gave up */
+    ENGRAM_ENOMEM = 6,      /* workspace too small */
+    ENGRAM_EUNSUPPORTED = 7 /* device is not sm_103 / feature missing */
+} engram_status;
+
+#define ENGRAM_N_TABLES 48
+#define ENGRAM_ROW_BYTES 256
+#define ENGRAM_MEM_DIM 512
+
+typedef struct {
+    int32_t vocab;   /* V: token ids must lie in [0, V); V itself is the pad id */
+    int32_t d_model; /* d: residual width; engram_fuse needs d % 256 == 0 */
+    int64_t rows;    /* R: rows per table, R >= 1, 48*R*256 bytes of table */
+    float rms_eps;   /* eps inside the rmsnorm of the gate (1e-6 by default) */
+    uint32_t reserved;
+    uint64_t seeds[ENGRAM_N_TABLES]; /* hash seed of table j */
+} engram_config;
+
+/* Human-readable name of a status code (static string). */
+const char *engram_status_string(engram_status st);
+
+/* Returns the sticky device error word of the current device as a status
+ * (ENGRAM_OK if clear) and clears it.  Synchronises the device. */
+engram_status engram_last_error(void);
+
+/*
+ * Row addresses: steps 1-2 above.  Addresses depend on token ids only (no
+ * table is read), so a whole prompt can be hashed before its forward pass
+ * ("What makes up the 511 GB of weights?": every address for a prompt can be
+ * computed up front and prefetched in one batch).
+ *   tokens      int32 [seq_offsets[n_seqs]] token ids in [0, V)
+ *   seq_offsets int64 [n_seqs+1] ascending; sequence s is
+ *               tokens[seq_offsets[s] .. seq_offsets[s+1])
+ *   last_n      0: query every position, in order, n_query must equal
+ *               seq_offsets[n_seqs] - seq_offsets[0];
+ *               k > 0: query the last k positions of each sequence, sequence
+ *               by sequence, n_query must equal n_seqs*k (a shorter sequence
+ *               sets ENGRAM_ERANGE on the device)
+ *   idx         int64 [n_query][48] output, row index in [0, R) of table j
+ */
+engram_status engram_hash(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                          int64_t n_seqs, int32_t last_n, int64_t n_query, int64_t *idx, void *stream);
+
+/*
+ * Step 3 (gather, dequantise, per-module sum).
+ *   tables int8 e4m3 codes [48][R][256], 16-byte aligned
+ *   scales fp32 [48][R]
+ *   idx    int64 [n_query][48], each in [0, R) (out-of-range rows read nothing
+ *          and set ENGRAM_ERANGE)
+ *   mem    fp32 [n_query][512] output, module 0 then module 1, 16-byte aligned
+ */
+engram_status engram_gather_reduce(const engram_config *cfg, const uint8_t *tables, const float *scales,
+                                   const int64_t *idx, int64_t n_query, float *mem, void *stream);
+
+/*
+ * Steps 4-5 (bf16 concat, tcgen05 projection, gated residual update in place).
+ *   mem   fp32 [n_query][512] (16-byte aligned)
+ *   W_out bf16 [512][d] row-major (16-byte aligned)
+ *   g     bf16 [d]
+ *   h     bf16 [n_query][d], read and updated in place (16-byte aligned)
+ * Needs d % 256 == 0.
+ */
+engram_status engram_fuse(const engram_config *cfg, const float *mem, const uint16_t *W_out, const uint16_t *g,
+                          uint16_t *h, int64_t n_query, void *stream);
+
+/*
+ * Steps 1-5 in one call on one stream (HBM-resident tables), as two kernels:
+ * a gather that hashes in registers (no idx array) and writes bf16 X, then
+ * the projection, which loads X by TMA.  workspace >=
+ * engram_forward_workspace_bytes(cfg, n_query) bytes of device memory,
+ * 256-byte aligned (it holds X); its contents are scratch.
+ */
+size_t engram_forward_workspace_bytes(const engram_config *cfg, int64_t n_query);
+engram_status engram_forward(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                             int64_t n_seqs, int32_t last_n, int64_t n_query, const uint8_t *tables,
+                             const float *scales, const uint16_t *W_out, const uint16_t *g, uint16_t *h,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The two halves of engram_forward, for callers that issue the table reads
+ * early (addresses depend on tokens only, so the gather can run before the
+ * layer that consumes it) and the projection later:
+ * engram_gather_x: steps 1-3 fused, hashing in registers, writing
+ *   X bf16 [n_query][512] (16-byte aligned) = bf16 of the module sums.
+ * engram_fuse_x:   steps 4-5 from that X (loaded by TMA); needs d % 256 == 0.
+ * engram_gather_x then engram_fuse_x gives the same bits as engram_forward.
+ */
+engram_status engram_gather_x(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                              int64_t n_seqs, int32_t last_n, int64_t n_query, const uint8_t *tables,
+                              const float *scales, uint16_t *X, void *stream);
+engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const uint16_t *W_out, const uint16_t *g,
+                            uint16_t *h, int64_t n_query, void *stream);
+
+/*
+ * Host-table path ("Engram: the table that is never multiplied": tables in
+ * pinned host memory read over unified addressing, the lookup on a side
+ * stream; "What makes up the 511 GB of weights?": addresses computed up front
+ * and prefetched in one batch).
+ *
+ * engram_dedup: the distinct (table, row) pairs among idx, sorted by
+ * (table, row), and each query's slot in that list.
+ *   workspace   >= engram_dedup_workspace_bytes(cfg) bytes, 256-byte aligned
+ *   unique      int64 [capacity] output: flat row j*R + row of slot u
+ *   idx_staged  int32 [n_query][48] output: slot of (t, j)
+ *   n_unique    int64 [1] output (device): number of distinct rows U; if
+ *               U > capacity only the first `capacity` slots are written, the
+ *               other queries point at slot 0 and ENGRAM_ECAPACITY is set.
+ */
+size_t engram_dedup_workspace_bytes(const engram_config *cfg);
+engram_status engram_dedup(const engram_config *cfg, const int64_t *idx, int64_t n_query, void *workspace,
+                           size_t workspace_bytes, int64_t *unique, int64_t capacity, int32_t *idx_staged,
+                           int64_t *n_unique, void *stream);
+
+/*
+ * engram_stage: copy the U = min(*n_unique, capacity) unique rows and their
+ * scales from host tables into device staging buffers.
+ *   host_tables e4m3 [48][R][256] in pinned host memory (16-byte aligned)
+ *   host_scales fp32 [48][R] in pinned host memory
+ *   staged_rows [capacity][256] and staged_scales [capacity] (device)
+ * Enqueued on `stream` (normally a side stream that waited for the dedup).
+ */
+engram_status engram_stage(const engram_config *cfg, const uint8_t *host_tables, const float *host_scales,
+                           const int64_t *unique, const int64_t *n_unique, int64_t capacity,
+                           uint8_t *staged_rows, float *staged_scales, void *stream);
+
+/*
+ * Step 3 over staged rows: same arithmetic, same summation order as
+ * engram_gather_reduce, so its output is bit-identical to the HBM path on
+ * the same inputs (SGLang's host-table mode is documented as bitwise
+ * identical, "Engram: the table that is never multiplied").
+ */
+engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_t *staged_rows,
+                                          const float *staged_scales, const int32_t *idx_staged,
+                                          int64_t n_query, int64_t capacity, float *mem, void *stream);
+
+/*
+ * The whole host-table path: hash and dedup on `stream`; the row stage on
+ * `side_stream` after `ev_dedup` (recorded here on `stream`); the staged
+ * gather and fuse on `stream` after `ev_staged` (recorded on `side_stream`).
+ * Both events are caller-created (cudaEventDisableTiming is fine).
+ * workspace >= engram_forward_host_workspace_bytes(cfg, n_query, capacity).
+ */
+size_t engram_forward_host_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t capacity);
+engram_status engram_forward_host(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
+                                  int64_t n_seqs, int32_t last_n, int64_t n_query, const uint8_t *host_tables,
+                                  const float *host_scales, const uint16_t *W_out, const uint16_t *g,
+                                  uint16_t *h, int64_t capacity, void *workspace, size_t workspace_bytes,
+                                  int64_t *n_unique, void *stream, void *side_stream, void *ev_dedup,
+                                  void *ev_staged);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H */

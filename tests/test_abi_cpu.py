@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and validates arguments before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "engram.h")
+
+
+@pytest.fixture(scope="module")
+def eg():
+    import engram_gram_hash_gb300 as eg
+    eg.build()
+    eg.lib()
+    return eg
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(engram_[a-z_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ["engram_hash", "engram_gather_reduce", "engram_fuse", "engram_forward", "engram_dedup",
+              "engram_stage", "engram_gather_reduce_staged", "engram_forward_host", "engram_last_error",
+              "engram_status_string"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(eg):
+    lib = ctypes.CDLL(eg.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in engram.h but not exported"
+
+
+def test_status_strings(eg):
+    for k in range(8):
+        assert eg.engram_status_string(k)
+    assert eg.engram_status_string(0) == "ok"
+
+
+def test_workspace_sizes(eg):
+    from synth.configs import CONFIGS, default_seeds
+
+    cfg = CONFIGS["large"]
+    c = eg.make_config(cfg.V, cfg.R, cfg.d, default_seeds())
+    ws = eg.engram_forward_workspace_bytes(c, cfg.tq)
+    assert ws >= cfg.tq * 512 * 2  # the bf16 X between the two kernels
+    d = eg.engram_dedup_workspace_bytes(c)
+    assert d >= 2 * 48 * cfg.R // 32 * 4
+    assert eg.engram_forward_host_workspace_bytes(c, 100, 4800) >= 4800 * 256
+
+
+def test_invalid_arguments_rejected_before_any_device_work(eg):
+    lib = eg.lib()
+    from synth.configs import default_seeds
+
+    c = eg.make_config(1024, 4096, 256, default_seeds())
+    null = ctypes.c_void_p(0)
+    # null config
+    assert lib.engram_hash(None, null, null, 1, 0, 10, null, null) == 1
+    # null buffers with work to do
+    assert lib.engram_hash(ctypes.byref(c), null, null, 1, 0, 10, null, null) == 1
+    assert lib.engram_gather_reduce(ctypes.byref(c), null, null, null, 10, null, null) == 1
+    # d not a multiple of 256
+    c2 = eg.make_config(1024, 4096, 200, default_seeds())
+    assert lib.engram_fuse(ctypes.byref(c2), ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                           ctypes.c_void_p(256), 4, null) == 1
+    # R < 1
+    c3 = eg.make_config(1024, 0, 256, default_seeds())
+    assert lib.engram_gather_reduce(ctypes.byref(c3), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                                    ctypes.c_void_p(256), 4, ctypes.c_void_p(256), null) == 1
+    # zero queries is a no-op that succeeds
+    assert lib.engram_hash(ctypes.byref(c), null, null, 1, 0, 0, null, null) == 0
+    assert lib.engram_gather_reduce(ctypes.byref(c), null, null, null, 0, null, null) == 0
+    # workspace too small
+    assert lib.engram_dedup(ctypes.byref(c), ctypes.c_void_p(256), 4, ctypes.c_void_p(256), 16,
+                            ctypes.c_void_p(256), 100, ctypes.c_void_p(256), ctypes.c_void_p(256), null) == 6
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The binding and the CUDA sources never reference oracle/."""
+    pkg = os.path.join(ROOT, "engram_gram_hash_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt and "oracle.c" not in txt, f

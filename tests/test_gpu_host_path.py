@@ -1,0 +1,117 @@
+"""The host-table path: dedup, staging from pinned host memory, and its
+output against the HBM path (bit-identical) and the oracle (needs a GB300)."""
+
+import numpy as np
+import pytest
+import torch
+
+from synth.configs import CONFIGS
+from workload import Workload, check_h, sample_queries
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eg():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    import engram_gram_hash_gb300 as eg
+
+    eg.lib()
+    return eg
+
+
+SMALL_HOST = CONFIGS["host"].with_(seq_lens=(700, 555), R=1 << 15, seed=9)
+
+
+def _unique_ref(idx, R):
+    flat = (np.arange(48)[None, :] * R + idx).reshape(-1)
+    return np.unique(flat)
+
+
+def test_dedup_matches_brute_force(eg):
+    w = Workload(SMALL_HOST, tables=False)
+    cfg = w.cfg
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    cap = cfg.tq * 48
+    unique, idx_staged, n_unique = eg.engram_dedup(w.c, idx, cap)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    ref_idx = w.ref_idx_all()
+    ref = _unique_ref(ref_idx, cfg.R)
+    U = int(n_unique.item())
+    assert U == len(ref)
+    assert np.array_equal(unique[:U].cpu().numpy(), ref)  # sorted by (table, row)
+    # every query's slot points back at its own (table, row)
+    back = unique[idx_staged.long()].cpu().numpy()
+    assert np.array_equal(back, np.arange(48)[None, :] * cfg.R + ref_idx)
+
+
+def test_dedup_capacity_overflow_is_reported(eg):
+    w = Workload(SMALL_HOST, tables=False)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    unique, idx_staged, n_unique = eg.engram_dedup(w.c, idx, 100)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 4
+    assert int(n_unique.item()) > 100
+    assert int(idx_staged.max().item()) < 100  # never points past the buffer
+
+
+def test_stage_copies_rows_byte_exact(eg):
+    w = Workload(SMALL_HOST, host_tables=True)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    cap = w.cfg.tq * 48
+    unique, idx_staged, n_unique = eg.engram_dedup(w.c, idx, cap)
+    rows, scales = eg.engram_stage(w.c, w.tables, w.scales, unique, n_unique, cap)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    U = int(n_unique.item())
+    u = unique[:U].cpu()
+    assert torch.equal(rows[:U].cpu(), w.tables.view(-1, 256)[u])
+    assert torch.equal(scales[:U].cpu(), w.scales.view(-1)[u])
+
+
+def test_host_path_bit_identical_to_hbm_path(eg):
+    """Same tables in pinned host memory and in HBM: the host-table forward
+    gives the same h bits as the HBM forward (the host-table mode is
+    documented as bitwise identical), and both match the oracle."""
+    w = Workload(SMALL_HOST, host_tables=True)
+    cfg = w.cfg
+    h_host = w.fresh_h()
+    side = torch.cuda.Stream()
+    n_unique = eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h_host,
+                                      capacity=cfg.tq * 48, side_stream=side)
+    dev_tables = w.tables.cuda()
+    dev_scales = w.scales.cuda()
+    h_hbm = w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, dev_tables, dev_scales, w.W, w.g, h_hbm)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_host.view(torch.int16), h_hbm.view(torch.int16))
+    assert int(n_unique.item()) == len(_unique_ref(w.ref_idx_all(), cfg.R))
+    q = sample_queries(cfg, w.offs, 200)
+    _, _, _, ref_h, _ = w.ref_for(q)
+    check_h(h_host[torch.from_numpy(q).cuda()], ref_h)
+
+
+def test_host_path_full_size(eg):
+    """The host-table workload at full size (51.5 GB of pinned tables)."""
+    cfg = CONFIGS["host"]
+    try:
+        w = Workload(cfg, host_tables=True)
+    except RuntimeError as e:  # pinning 53 GB can fail on a small host
+        pytest.skip(f"cannot pin {cfg.table_bytes / 1e9:.1f} GB of host memory: {e}")
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    cap = cfg.tq * 48
+    h = w.fresh_h()
+    n_unique = eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, capacity=cap)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    ref_idx = w.ref_idx_all()
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert int(n_unique.item()) == len(_unique_ref(ref_idx, cfg.R))
+    q = sample_queries(cfg, w.offs, 200)
+    _, _, _, ref_h, _ = w.ref_for(q)
+    check_h(h[torch.from_numpy(q).cuda()], ref_h)
+    del w, h, idx
+    torch.cuda.empty_cache()

@@ -1,0 +1,241 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs a GB300)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import device as sd
+from synth import host
+from synth.configs import CONFIGS
+from workload import Workload, bf16_to_f64, check_h, check_mem, sample_queries
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eg():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    import engram_gram_hash_gb300 as eg
+
+    eg.lib()  # fail loudly when the CUDA library is missing
+    return eg
+
+
+SMALL = {
+    "tiny": CONFIGS["tiny"],
+    # ragged sequences (lengths 1 and 2 exercise the pad), prime R
+    "ragged_prime": CONFIGS["tiny"].with_(seq_lens=(300, 1, 2, 140, 77), R=4093, seed=5),
+    # d = 4096, several 128-token tiles plus a ragged tail, repeated spans
+    "prefill_small": CONFIGS["prefill"].with_(seq_lens=(640, 421), R=1 << 16, seed=6),
+    # decode: 64 sequences of 4 tokens, only the last one queried
+    "decode_small": CONFIGS["decode"].with_(R=1 << 16),
+    # d = 512 (two 256-column chunks)
+    "d512": CONFIGS["tiny"].with_(d=512, seq_lens=(333,), seed=7),
+}
+
+
+def _clear(eg):
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_hash_bit_exact_small(eg, name):
+    w = Workload(SMALL[name], tables=False)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=w.cfg.last_n)
+    _clear(eg)
+    assert np.array_equal(idx.cpu().numpy(), w.ref_idx_all())
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_gather_reduce_small(eg, name):
+    w = Workload(SMALL[name])
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=w.cfg.last_n)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    _clear(eg)
+    q = np.arange(w.cfg.tq)
+    ridx, rmem, bound, _, _ = w.ref_for(q)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    check_mem(mem.cpu().numpy(), rmem, bound)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_fuse_small(eg, name):
+    """engram_fuse alone: the oracle's mem (as fp32) in, h compared with the
+    oracle's fuse of the same fp32 mem."""
+    w = Workload(SMALL[name], tables=False)
+    cfg = w.cfg
+    rng = np.random.default_rng(cfg.seed)
+    mem32 = (rng.standard_normal((cfg.tq, 512)) * 6.0).astype(np.float32)
+    h = w.fresh_h()
+    eg.engram_fuse(w.c, torch.from_numpy(mem32).cuda(), w.W, w.g, h)
+    _clear(eg)
+    h0 = host.h_rows(cfg.seed, cfg.d, np.arange(cfg.tq))
+    ref, _ = oracle.fuse(mem32.astype(np.float64), host.w_out(cfg.seed, cfg.d), host.g_vec(cfg.seed, cfg.d), h0,
+                         cfg.rms_eps)
+    check_h(h, ref)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small(eg, name):
+    """The one-call path against the oracle on every query token, and against
+    the three separate calls (same kernels' arithmetic: bit-identical)."""
+    w = Workload(SMALL[name])
+    h = w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, last_n=w.cfg.last_n)
+    h2 = w.fresh_h()
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=w.cfg.last_n)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    eg.engram_fuse(w.c, mem, w.W, w.g, h2)
+    _clear(eg)
+    assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+    _, _, _, ref_h, _ = w.ref_for(np.arange(w.cfg.tq))
+    check_h(h, ref_h)
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_small", "decode_small"])
+def test_split_halves_equal_forward(eg, name):
+    """engram_gather_x then engram_fuse_x gives engram_forward's bits, and X
+    is bf16 of the fp32 module sums of engram_gather_reduce."""
+    w = Workload(SMALL[name])
+    X = eg.engram_gather_x(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, last_n=w.cfg.last_n)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=w.cfg.last_n)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    h1, h2 = w.fresh_h(), w.fresh_h()
+    eg.engram_fuse_x(w.c, X, w.W, w.g, h1)
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h2, last_n=w.cfg.last_n)
+    _clear(eg)
+    assert torch.equal(X.view(torch.int16), mem.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+
+
+def test_generator_twin_rows_match_host(eg):
+    """The device-filled tables/scales/h equal the host draws bit for bit."""
+    cfg = SMALL["ragged_prime"]
+    w = Workload(cfg)
+    rng = np.random.default_rng(1)
+    j = rng.integers(0, 48, 200)
+    r = rng.integers(0, cfg.R, 200)
+    got = w.tables[torch.from_numpy(j).cuda(), torch.from_numpy(r).cuda()].cpu().numpy()
+    assert np.array_equal(got, host.table_rows(cfg.seed, j, r))
+    gs = w.scales[torch.from_numpy(j).cuda(), torch.from_numpy(r).cuda()].cpu().numpy()
+    assert np.array_equal(gs, host.scales(cfg.seed, j, r))
+    h = w.fresh_h()
+    assert np.array_equal(h.view(torch.int16).cpu().numpy().view(np.uint16), host.h_rows(cfg.seed, cfg.d, np.arange(cfg.tq)))
+    assert np.array_equal(w.W.view(torch.int16).cpu().numpy().view(np.uint16), host.w_out(cfg.seed, cfg.d))
+
+
+def test_idx_independent_of_tables(eg):
+    """Row addresses depend on token ids only: the hash takes no table, and
+    overwriting every table leaves the gathered rows' addresses unchanged."""
+    w = Workload(SMALL["tiny"])
+    idx1 = eg.engram_hash(w.c, w.tokens, w.seq_offsets).clone()
+    w.tables.random_(0, 127)
+    idx2 = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    _clear(eg)
+    assert torch.equal(idx1, idx2)
+
+
+def test_special_cases_on_gpu(eg):
+    """All rows = e4m3 1.0 with unit scales: every mem entry is exactly 24;
+    g = 0 gives gate 1/2; W_out = 0 leaves h bit-unchanged."""
+    w = Workload(SMALL["tiny"])
+    w.tables.fill_(0x38)
+    w.scales.fill_(1.0)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    h = w.fresh_h()
+    h0 = h.clone()
+    eg.engram_fuse(w.c, mem, torch.zeros_like(w.W), w.g, h)
+    _clear(eg)
+    assert torch.all(mem == 24.0)
+    assert torch.equal(h.view(torch.int16), h0.view(torch.int16))
+    # g = 0: gate = 1/2 exactly, so h = bf16(h + y/2) with y = 24 * colsum(W)
+    h = w.fresh_h()
+    eg.engram_fuse(w.c, mem, w.W, torch.zeros_like(w.g), h)
+    _clear(eg)
+    cfg = w.cfg
+    ref, gate = oracle.fuse(np.full((cfg.tq, 512), 24.0), host.w_out(cfg.seed, cfg.d), np.zeros(cfg.d, np.uint16),
+                            host.h_rows(cfg.seed, cfg.d, np.arange(cfg.tq)))
+    assert np.all(gate == 0.5)
+    check_h(h, ref)
+
+
+def test_empty_and_invalid_arguments(eg):
+    w = Workload(SMALL["tiny"])
+    e = torch.empty((0, 48), dtype=torch.int64, device="cuda")
+    out = eg.engram_gather_reduce(w.c, w.tables, w.scales, e)
+    assert out.shape == (0, 512)
+    h = torch.empty((0, w.cfg.d), dtype=torch.bfloat16, device="cuda")
+    eg.engram_fuse(w.c, torch.empty((0, 512), device="cuda"), w.W, w.g, h)
+    bad = eg.make_config(w.cfg.V, w.cfg.R, 200, w.seeds)  # d not a multiple of 256
+    hb = torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(eg.EngramError) as ex:
+        eg.engram_fuse(bad, torch.zeros((4, 512), device="cuda"), torch.zeros((512, 200), dtype=torch.bfloat16,
+                       device="cuda"), torch.zeros(200, dtype=torch.bfloat16, device="cuda"), hb)
+    assert ex.value.status == 1
+    with pytest.raises(eg.EngramError) as ex:  # misaligned tables
+        eg.engram_gather_reduce(w.c, w.tables.view(-1)[1:1 + 48 * 10 * 256].view(48, 10, 256), w.scales,
+                                torch.zeros((1, 48), dtype=torch.int64, device="cuda"))
+    assert ex.value.status == 1
+    with pytest.raises(eg.EngramError) as ex:  # workspace too small
+        eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, w.fresh_h(),
+                          workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert ex.value.status == 6
+    with pytest.raises(eg.EngramError):  # last_n > 0 with the wrong query count
+        eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=2, n_query=5)
+    _clear(eg)
+
+
+def test_device_range_errors_are_reported(eg):
+    """Conditions only the device sees set the sticky error word (no trap)."""
+    w = Workload(SMALL["tiny"])
+    tok = w.tokens.clone()
+    tok[5] = w.cfg.V  # the pad id is not a valid token
+    eg.engram_hash(w.c, tok, w.seq_offsets)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 3
+    assert eg.engram_last_error() == 0  # cleared
+    idx = torch.full((3, 48), w.cfg.R, dtype=torch.int64, device="cuda")  # row index == R
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 3
+    assert torch.all(mem == 0)  # out-of-range rows read nothing
+    offs = torch.tensor([0, 1, 512], dtype=torch.int64, device="cuda")  # a 1-token sequence with last_n = 2
+    eg.engram_hash(w.c, w.tokens, offs, last_n=2)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 3
+
+
+# ------------------------------------------------------------- full sizes ---
+
+FULL = ["tiny", "decode", "prefill", "large"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_forward(eg, name):
+    """The workloads at their full sizes, in the launch configuration the
+    benchmark times (engram_forward on one stream): idx on every query token,
+    mem and h on a seeded sample plus every sequence start and the last token."""
+    cfg = CONFIGS[name]
+    free, _ = torch.cuda.mem_get_info()
+    need = cfg.table_bytes * 1.02 + cfg.tq * (cfg.d * 2 * 2 + 512 * 8 + 48 * 8) + (1 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.1f} GB of device memory, {free / 1e9:.1f} GB free")
+    w = Workload(cfg)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=cfg.last_n)
+    _clear(eg)
+    assert np.array_equal(idx.cpu().numpy(), w.ref_idx_all())
+    q = sample_queries(cfg, w.offs, 256 if cfg.d > 256 else cfg.tq)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    h = w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, last_n=cfg.last_n)
+    _clear(eg)
+    qt = torch.from_numpy(q).cuda()
+    _, rmem, bound, rh, _ = w.ref_for(q)
+    check_mem(mem[qt].cpu().numpy(), rmem, bound)
+    check_h(h[qt], rh)
+    del w, idx, mem, h
+    torch.cuda.empty_cache()
