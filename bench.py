@@ -3,8 +3,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of the workload:
-engram_hash -> engram_gather_reduce -> engram_fuse through the C ABI (the
-same kernels engram_forward launches), h updated in place.  Inputs are
+engram_gather_x (n-gram hash in registers + row gather + dequant + module
+sums -> bf16 X) then engram_fuse_x (tcgen05 projection + gated residual
+update, h in place) through the C ABI -- the two kernels engram_forward
+launches, called separately so each is timed with CUDA events.  The
+host-table workload runs engram_forward_host (hash, dedup, staging from
+pinned host memory on a side stream, staged gather, projection).  Inputs are
 resident in HBM when the timed region starts and are larger than L2 (tables
 of 13-103 GB, h of 0.5-2 GB), so no L2 flush is needed between steps.
 
@@ -46,11 +50,10 @@ def measured_peaks():
 
 
 # Algorithmic bytes per query token of each kernel (what the method must move):
-#   hash:   4 B of token id in, 48 x 8 B of row index out
-#   gather: 48 x 256 B of rows + 48 x 4 B of scales + 384 B of idx in, 512 x 4 B of mem out
-#   fuse:   512 x 4 B of mem in, d x 2 B of h in, d x 2 B of h out
+#   gather: 4 B of token id + 48 x 256 B of rows + 48 x 4 B of scales in, 512 x 2 B of X out
+#   fuse:   512 x 2 B of X in, d x 2 B of h in, d x 2 B of h out
 def kernel_bytes_per_token(d):
-    return {"hash": 4 + 48 * 8, "gather": 48 * 256 + 48 * 4 + 48 * 8 + 512 * 4, "fuse": 512 * 4 + 4 * d}
+    return {"gather": 4 + 48 * 256 + 48 * 4 + 512 * 2, "fuse": 512 * 2 + 4 * d}
 
 
 def nominal_bytes_per_token(d):
@@ -94,7 +97,7 @@ def smi_index(local_rank):
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,16 +105,26 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = os.path.join("/tmp", f"engram_clocks_{os.getpid()}.csv")
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while os.path.getsize(self.path) == 0 and time.time() - t0 < 5:  # sampler is up before timing
+                time.sleep(0.05)
         except OSError:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -125,7 +138,9 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
+        from datetime import datetime
+
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -133,19 +148,23 @@ class ClockSampler:
                 if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]),
+                                 [nm for nm, v in zip(names, parts[5:9]) if v.lower() == "active"]))
                 except ValueError:
                     continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
         os.unlink(self.path)
-        if not sm:
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        busy = [x for x in sm if x > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        window = "timed region"
+        sel = [r for r in rows if self.t_start is not None and self.t_start - 0.05 <= r[0] <= self.t_end + 0.05]
+        if len(sel) < 2:  # a timed region shorter than the sampling period: use the nearest samples
+            window = "timed region too short for 100 ms sampling; samples nearest to it"
+            mid = 0.5 * (self.t_start + self.t_end) if self.t_start else rows[-1][0]
+            sel = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
+        reasons = sorted({x for r in sel for x in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel), "window": window}
 
 
 # --------------------------------------------------------------- our arm ----
@@ -163,6 +182,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     eg.lib()
     base = CONFIGS[args.workload]
+    if args.rows:
+        base = base.with_(R=args.rows)
+    if args.tokens:
+        base = base.with_(seq_lens=tuple(min(L, args.tokens) for L in base.seq_lens))
     # weak scaling: rank r draws its own token batch (tables are replicated weights)
     cfg = base.with_(seed=base.seed) if rank == 0 else base.with_(seed=base.seed + 1000 * rank)
     seeds = default_seeds()
@@ -185,8 +208,7 @@ def run_ours(args, rank, world, local_rank):
     sd.fill_g(g, base.seed)
     sd.fill_h(h, cfg.seed)
     nq = cfg.tq
-    idx = torch.empty((nq, 48), dtype=torch.int64, device=dev)
-    mem = torch.empty((nq, 512), dtype=torch.float32, device=dev)
+    X = torch.empty((nq, 512), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
@@ -200,22 +222,23 @@ def run_ours(args, rank, world, local_rank):
 
     def step(ev=None):
         if host:
+            if ev is not None:
+                ev[0].record(stream)
             eg.engram_forward_host(c, tokens, seq_offsets, tables, scales, W, g, h, cap, last_n=cfg.last_n,
                                    n_query=nq, workspace=fws, n_unique=n_unique, side_stream=side, ev_dedup=ev_a,
                                    ev_staged=ev_b)
-            return 1
+            if ev is not None:
+                ev[1].record(stream)
+            return 9  # hash, 5 dedup kernels, stage, staged gather, fuse
         if ev is not None:
             ev[0].record(stream)
-        eg.engram_hash(c, tokens, seq_offsets, last_n=cfg.last_n, n_query=nq, idx=idx)
+        eg.engram_gather_x(c, tokens, seq_offsets, tables, scales, last_n=cfg.last_n, n_query=nq, X=X)
         if ev is not None:
             ev[1].record(stream)
-        eg.engram_gather_reduce(c, tables, scales, idx, mem=mem)
+        eg.engram_fuse_x(c, X, W, g, h)
         if ev is not None:
             ev[2].record(stream)
-        eg.engram_fuse(c, mem, W, g, h)
-        if ev is not None:
-            ev[3].record(stream)
-        return 3
+        return 2
 
     for _ in range(args.warmup):
         step()
@@ -224,18 +247,20 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device error during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(smi_index(local_rank)) as cs:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        cs.mark_start()
         t0.record(stream)
         for k in range(K):
-            launches += step(None if host else evs[k])
+            launches += step(evs[k])
         t1.record(stream)
         torch.cuda.synchronize()
+        cs.mark_end()
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1)
@@ -252,9 +277,8 @@ def run_ours(args, rank, world, local_rank):
     per_kernel_ms = {}
     if not host:
         per_kernel_ms = {
-            "hash": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
-            "gather": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
-            "fuse": sum(e[2].elapsed_time(e[3]) for e in evs) / K,
+            "gather": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
+            "fuse": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
         }
     kb = kernel_bytes_per_token(cfg.d)
     kernels = {}
@@ -271,6 +295,9 @@ def run_ours(args, rank, world, local_rank):
                     "algorithmic_bytes_per_launch": kb[dom] * nq,
                     "peak_src": f"{peaks['src']} hbm_gbs (burst copy)"}
 
+    if host:
+        roofline = host_link_roofline(eg, c, cfg, tokens, seq_offsets, tables, scales, nq, dev)
+
     tokens_total = nq * world
     value = tokens_total / (ms_max * 1e-3 / K)
     step_gbs = nominal_bytes_per_token(cfg.d) * nq / (ms_max * 1e-3 / K) / 1e9
@@ -279,7 +306,7 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3->f32 gather, bf16 x bf16 -> f32 projection, bf16 residual",
         "data": "synthetic (seeded; tables e4m3 ~ quantised N(0,1), per-row fp32 scales U[0.5,2])",
-        "config": {"workload": args.workload, "V": cfg.V, "R": cfg.R, "n_seqs": cfg.n_seqs,
+        "config": {"workload": args.workload + (" (reduced)" if args.rows or args.tokens else ""), "V": cfg.V, "R": cfg.R, "n_seqs": cfg.n_seqs,
                    "tokens_per_step_per_gpu": cfg.t_all, "query_tokens_per_step_per_gpu": nq, "d_model": cfg.d,
                    "table_bytes": cfg.table_bytes, "tables_in": "pinned host" if host else "HBM",
                    "token_ids": ("uniform" if cfg.zipf_s == 0 else f"Zipf({cfg.zipf_s})"),
@@ -290,10 +317,53 @@ def run_ours(args, rank, world, local_rank):
     }
     if host:
         out["config"]["n_unique_rows"] = int(n_unique.item())
-    out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
+    if not args.no_e2e:
+        out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     return out
+
+
+def host_link_roofline(eg, c, cfg, tokens, seq_offsets, tables, scales, nq, dev):
+    """The staging kernel of the host-table path against the measured host
+    link: unique rows x (256 B row + 4 B scale) moved over the link, divided
+    by the stage kernel's CUDA-event time, against a pinned host-to-device
+    copy of 2 GB measured here (cudaMemcpyAsync)."""
+    import torch
+
+    idx = eg.engram_hash(c, tokens, seq_offsets, last_n=cfg.last_n, n_query=nq)
+    cap = nq * 48
+    unique, idx_staged, n_unique = eg.engram_dedup(c, idx, cap)
+    rows = torch.empty((cap, 256), dtype=torch.uint8, device=dev)
+    scs = torch.empty(cap, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    for _ in range(2):
+        eg.engram_stage(c, tables, scales, unique, n_unique, cap, rows, scs)
+    reps = 10
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        eg.engram_stage(c, tables, scales, unique, n_unique, cap, rows, scs)
+    b.record(st)
+    torch.cuda.synchronize()
+    stage_ms = a.elapsed_time(b) / reps
+    U = int(n_unique.item())
+    link_bytes = U * (256 + 4)
+    # measured host link: pinned H2D copy
+    src = torch.empty(1 << 31, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    a.record(st)
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    b.record(st)
+    torch.cuda.synchronize()
+    h2d_gbs = 3 * (1 << 31) / (a.elapsed_time(b) * 1e-3) / 1e9
+    ach = link_bytes / (stage_ms * 1e-3) / 1e9
+    return {"kernel": "stage", "bound": "host-link", "achieved": round(ach, 1), "peak": round(h2d_gbs, 1),
+            "unit": "GB/s", "frac": round(ach / h2d_gbs, 4), "traffic": None,
+            "algorithmic_bytes_per_launch": link_bytes, "unique_rows": U, "stage_ms": round(stage_ms, 4),
+            "peak_src": "measured here: pinned host-to-device cudaMemcpyAsync of 2 GiB"}
 
 
 def e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h_dev, nq, dev, world):
@@ -332,7 +402,7 @@ def e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h_dev,
     for _ in range(max(1, args.warmup)):
         one()
     torch.cuda.synchronize()
-    K = args.steps
+    K = args.e2e_steps
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -428,15 +498,58 @@ def run_reference(args, rank, world):
     }
 
 
+def run_probe(args):
+    """Ceilings for the gather: random 256-byte rows over a large buffer, with
+    and without one 4-byte scale per row from a second array."""
+    import ctypes
+
+    import torch
+
+    lib = ctypes.CDLL(os.path.join(ROOT, "libbench_probes.so"))
+    lib.probe_random_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
+    n_rows = 1 << ((args.probe_gb << 30) // 256).bit_length() - 1  # power of two
+    rows = torch.empty(n_rows * 256, dtype=torch.uint8, device="cuda")
+    rows.fill_(1)
+    scales = torch.ones(n_rows, dtype=torch.float32, device="cuda")
+    sink = torch.zeros(1, device="cuda")
+    n_warps = 262144  # 24 rows per warp: 6.3 M rows = 1.6 GB per launch
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = {"probe": "random 256-byte rows", "buffer_GB": args.probe_gb, "rows_per_launch": n_warps * 24}
+    for name, sc in (("rows", None), ("rows+scales", scales)):
+        scp = ctypes.c_void_p(sc.data_ptr() if sc is not None else 0)
+        for k in range(3):
+            lib.probe_random_rows(ctypes.c_void_p(rows.data_ptr()), scp, n_rows, n_warps, k, ctypes.c_void_p(sink.data_ptr()), st)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record()
+        for k in range(reps):
+            lib.probe_random_rows(ctypes.c_void_p(rows.data_ptr()), scp, n_rows, n_warps, 100 + k,
+                                  ctypes.c_void_p(sink.data_ptr()), st)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        useful = n_warps * 24 * (256 + (4 if sc is not None else 0))
+        out[name] = {"ms": round(ms, 4), "useful_GBps": round(useful / ms / 1e6, 1),
+                     "frac_of_copy_peak": round(useful / ms / 1e6 / measured_peaks()["hbm_gbs"], 3)}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large", choices=["tiny", "decode", "prefill", "large", "host"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--probe", action="store_true", help="print the random-row bandwidth ceilings and exit")
+    ap.add_argument("--probe-gb", type=int, default=32)
+    ap.add_argument("--rows", type=int, default=0, help="override R (reduced case for profiling)")
+    ap.add_argument("--tokens", type=int, default=0, help="override tokens per sequence (reduced case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3  # at least three warm-up steps
@@ -444,6 +557,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.probe:
+        print(json.dumps(run_probe(args)), flush=True)
+        return
     if args.impl == "reference":
         if rank != 0:
             return

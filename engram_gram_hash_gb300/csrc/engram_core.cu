@@ -181,9 +181,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     for (int i = 0; i < 12; ++i) {
         const int src = 2 * i + half;
         const int64_t o = __shfl_sync(0xffffffffu, off, src);
-        const int k = __shfl_sync(0xffffffffu, ok, src);
         s[i] = __shfl_sync(0xffffffffu, sc, src);
-        v[i] = k ? ld_nc_na_v4(P.rows + o + c16 * 16) : make_uint4(0, 0, 0, 0);
+        v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 ...
+        if (!__shfl_sync(0xffffffffu, ok, src)) v[i] = make_uint4(0, 0, 0, 0);  // ... and is dropped
     }
     float acc[16];
 #pragma unroll
@@ -567,24 +567,35 @@ static bool bf16_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64
 }
 
 // CTAs per cluster (d slices) for a projection of m_tiles tiles and n_chunks
-// 256-column chunks: few tiles spread d over up to 8 CTAs; many tiles use
-// slices of at most 4 chunks so each CTA's h slice stays small in L2.
+// 256-column chunks.  A slice must be 1, 2, 4, 8 or 16 chunks (the kernel's
+// CPG) and a cluster at most 8 CTAs.  Many tiles: slices of 4 chunks (each
+// CTA's h slice stays small in L2, clusters stay small).  Few tiles: spread
+// d over as many CTAs as fit.  Returns 0 if d has no valid split.
 static int pick_groups(int64_t m_tiles, int n_chunks) {
-    int g = 1;
     const int sms = num_sms();
-    if (m_tiles * 2 < sms) {
-        while (g * 2 <= fuse::MAX_GROUPS && n_chunks % (g * 2) == 0 && m_tiles * g * 2 <= sms) g *= 2;
-    } else {
-        while (n_chunks / g > 4 && g * 2 <= fuse::MAX_GROUPS && n_chunks % (g * 2) == 0) g *= 2;
+    int best = 0;
+    double best_score = 1e30;
+    for (int g = 1; g <= fuse::MAX_GROUPS; ++g) {
+        if (n_chunks % g) continue;
+        const int cpg = n_chunks / g;
+        if (cpg != 1 && cpg != 2 && cpg != 4 && cpg != 8 && cpg != 16) continue;
+        double score;
+        if (m_tiles * 2 >= sms)
+            score = fabs(log2((double)cpg) - 2.0) * 100.0 + g;  // prefer 4 chunks per CTA, then fewer CTAs
+        else
+            score = (m_tiles * g <= sms ? 0.0 : 1000.0) - g;     // prefer more CTAs while they fit
+        if (score < best_score) {
+            best_score = score;
+            best = g;
+        }
     }
-    while (n_chunks / g > 16 && g * 2 <= fuse::MAX_GROUPS && n_chunks % (g * 2) == 0) g *= 2;
-    return g;
+    return best;
 }
 
-template <int XSRC>
+template <int XSRC, int CPG>
 static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
                                    cudaStream_t st) {
-    auto kern = fuse::fuse_kernel<XSRC>;
+    auto kern = fuse::fuse_kernel<XSRC, CPG>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -623,6 +634,19 @@ static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &x
     return launch_status();
 }
 
+template <int XSRC>
+static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
+                                   cudaStream_t st) {
+    switch (p.cpg) {
+        case 1: return fuse_launch_t<XSRC, 1>(wmap, xmap, p, st);
+        case 2: return fuse_launch_t<XSRC, 2>(wmap, xmap, p, st);
+        case 4: return fuse_launch_t<XSRC, 4>(wmap, xmap, p, st);
+        case 8: return fuse_launch_t<XSRC, 8>(wmap, xmap, p, st);
+        case 16: return fuse_launch_t<XSRC, 16>(wmap, xmap, p, st);
+    }
+    return ENGRAM_EINVAL;
+}
+
 // y = X @ W_out and the gated residual update.  X comes either from fp32 mem
 // (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
 engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint16_t *x_bf16, const uint16_t *W,
@@ -637,6 +661,7 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     p.m_tiles = (n_query + fuse::BM - 1) / fuse::BM;
     p.d = d;
     p.groups = pick_groups(p.m_tiles, n_chunks);
+    if (p.groups == 0) return ENGRAM_EINVAL;
     p.cpg = n_chunks / p.groups;
     p.eps = cfg->rms_eps;
     p.inv_sqrt_d = 1.0f / sqrtf((float)d);
@@ -647,9 +672,9 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     if (x_bf16) {
         if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
             return cuda_fail(cudaErrorInvalidValue, "X tensor map");
-        return fuse_launch_t<fuse::X_FROM_BF16_TMA>(wmap, xmap, p, st);
+        return fuse_dispatch<fuse::X_FROM_BF16_TMA>(wmap, xmap, p, st);
     }
-    return fuse_launch_t<fuse::X_FROM_F32_MEM>(wmap, xmap, p, st);
+    return fuse_dispatch<fuse::X_FROM_F32_MEM>(wmap, xmap, p, st);
 }
 
 engram_status check_fuse_args(const engram_config *cfg, const void *W, const void *g, const void *h) {
