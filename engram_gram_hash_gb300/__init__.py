@@ -84,6 +84,7 @@ def lib():
             "engram_forward": ([C, P, P, i64, i32, i64, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "engram_gather_x": ([C, P, P, i64, i32, i64, P, P, P, P], ctypes.c_int),
             "engram_fuse_x": ([C, P, P, P, P, i64, P], ctypes.c_int),
+            "engram_forward_no_workspace": ([C, P, P, i64, i32, i64, P, P, P, P, P, P], ctypes.c_int),
             "engram_dedup_workspace_bytes": ([C], sz),
             "engram_dedup": ([C, P, i64, P, sz, P, i64, P, P, P], ctypes.c_int),
             "engram_stage": ([C, P, P, P, P, i64, P, P, P], ctypes.c_int),
@@ -211,6 +212,32 @@ def engram_forward(cfg, tokens, seq_offsets, tables, scales, W_out, g, h, last_n
                              _ptr(tables), _ptr(scales), _ptr(W_out), _ptr(g), _ptr(h), _ptr(workspace),
                              workspace.numel(), _stream(stream)),
         "engram_forward",
+    )
+    return h
+
+
+NO_WORKSPACE_MAX_QUERY = 16384
+
+
+def engram_forward_no_workspace(cfg, tokens, seq_offsets, tables, scales, W_out, g, h, last_n=0, n_query=None,
+                                stream=None):
+    """engram_forward with its scratch in the library's own device array (no
+    workspace argument, nothing allocated): for callers that cannot allocate
+    device memory.  At most NO_WORKSPACE_MAX_QUERY query tokens per call;
+    calls that overlap on the GPU share the array and race."""
+    _need(tokens, torch.int32, "tokens")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(tables, torch.uint8, "tables")
+    _need(scales, torch.float32, "scales")
+    _need(W_out, torch.bfloat16, "W_out")
+    _need(g, torch.bfloat16, "g")
+    _need(h, torch.bfloat16, "h")
+    nq = _n_query(tokens, seq_offsets, last_n, n_query)
+    _check(
+        lib().engram_forward_no_workspace(ctypes.byref(cfg), _ptr(tokens), _ptr(seq_offsets), seq_offsets.numel() - 1,
+                                          last_n, nq, _ptr(tables), _ptr(scales), _ptr(W_out), _ptr(g), _ptr(h),
+                                          _stream(stream)),
+        "engram_forward_no_workspace",
     )
     return h
 

@@ -10,6 +10,7 @@
 // side stream, bitwise-identical host-table mode).
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 #include <cstdlib>
 #include <cstring>
 
@@ -895,6 +896,63 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
     if (cudaEventRecord((cudaEvent_t)ev_staged, side) != cudaSuccess) return ENGRAM_ECUDA;
     if (cudaStreamWaitEvent(st, (cudaEvent_t)ev_staged, 0) != cudaSuccess) return ENGRAM_ECUDA;
     s = gather_launch(IDX_STAGED_I32, true, rows, sc, idx_staged, nullptr, n_query, capacity, X, st);
+    if (s != ENGRAM_OK) return s;
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
+}
+
+// ====================================================== no-workspace variant ==
+// engram_forward for callers that cannot allocate device memory (see the
+// header): the bf16 X handed from the gather kernel to the projection lives in
+// this file-scope array instead of a caller workspace.  Every GPU that loads
+// the library holds it (16 MB) until the process exits, and every call shares
+// it.
+
+static __device__ __align__(256) uint16_t g_no_workspace_x[ENGRAM_NO_WORKSPACE_MAX_QUERY * ENGRAM_MEM_DIM];
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, never a device address, so it
+// is looked up once per device (with that device current) and cached.
+static engram_status no_workspace_scratch(uint16_t **out) {
+    static std::mutex mu;
+    static uint16_t *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return ENGRAM_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_no_workspace_x);
+        if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(no-workspace scratch)");
+        addr[dev] = static_cast<uint16_t *>(p);
+    }
+    *out = addr[dev];
+    return ENGRAM_OK;
+}
+
+extern "C" engram_status engram_forward_no_workspace(const engram_config *cfg, const int32_t *tokens,
+                                                     const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                                     int64_t n_query, const uint8_t *tables, const float *scales,
+                                                     const uint16_t *W_out, const uint16_t *g, uint16_t *h,
+                                                     void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY) return ENGRAM_ENOMEM;  // past the built-in scratch
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales) return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(tokens, 4) || !aligned(seq_offsets, 8))
+        return ENGRAM_EINVAL;
+    uint16_t *X = nullptr;
+    engram_status s = no_workspace_scratch(&X);
+    if (s != ENGRAM_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    HashParams hp;
+    fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
+    // X rows [0, n_query) are all written before the projection reads them,
+    // and the projection's tensor map stops at n_query rows: nothing left in
+    // the array by an earlier call is read, so nothing needs clearing.
+    s = gather_launch(IDX_HASH, true, tables, scales, nullptr, &hp, n_query, cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
 }

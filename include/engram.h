@@ -147,6 +147,35 @@ engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const u
                             uint16_t *h, int64_t n_query, void *stream);
 
 /*
+ * engram_forward without a workspace argument.  The sources have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- code running inside a host engine or framework that owns
+ * all device memory through its own pool and forbids raw cudaMalloc from
+ * plug-ins, or that may not allocate once it is serving (an allocation there
+ * can fail, fragment the pool or stall other work).  It does the same work as
+ * engram_forward, with the bf16 X between its two kernels kept in a
+ * file-scope device array of ENGRAM_NO_WORKSPACE_MAX_QUERY x 512 bf16
+ * (16 MB) instead of a caller workspace.
+ *   - Allocates nothing and calls no allocating CUDA or library routine.
+ *   - Every GPU that loads libengram.so holds that array until the process
+ *     exits.
+ *   - n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY returns ENGRAM_ENOMEM and
+ *     enqueues nothing; other arguments are checked as for engram_forward.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture on the device.
+ *   - Every call shares the one array: two calls that overlap on the GPU
+ *     (different streams, or different host threads on one device) race on
+ *     it and give undefined results.  Calls in one stream are ordered and
+ *     safe.  Nothing in the array needs clearing between calls.
+ */
+#define ENGRAM_NO_WORKSPACE_MAX_QUERY 16384
+engram_status engram_forward_no_workspace(const engram_config *cfg, const int32_t *tokens,
+                                          const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                          int64_t n_query, const uint8_t *tables, const float *scales,
+                                          const uint16_t *W_out, const uint16_t *g, uint16_t *h, void *stream);
+
+/*
  * Host-table path ("Engram: the table that is never multiplied": tables in
  * pinned host memory read over unified addressing, the lookup on a side
  * stream; "What makes up the 511 GB of weights?": addresses computed up front
