@@ -189,18 +189,22 @@ def run_ours(args, rank, world, local_rank):
     # weak scaling: rank r draws its own token batch (tables are replicated weights)
     cfg = base.with_(seed=base.seed) if rank == 0 else base.with_(seed=base.seed + 1000 * rank)
     seeds = default_seeds()
-    c = eg.make_config(cfg.V, cfg.R, cfg.d, seeds, cfg.rms_eps)
+    record = args.layout == "record"
+    c = eg.make_config(cfg.V, cfg.R, cfg.d, seeds, cfg.rms_eps,
+                       row_layout=eg.ROWS_RECORD if record else eg.ROWS_SEPARATE)
     tok, offs = make_tokens(cfg)
     tokens = torch.from_numpy(tok).to(dev)
     seq_offsets = torch.from_numpy(offs).to(dev)
-    if cfg.host_tables:
-        tables = torch.empty((48, cfg.R, 256), dtype=torch.uint8, pin_memory=True)
-        scales = torch.empty((48, cfg.R), dtype=torch.float32, pin_memory=True)
-    else:
-        tables = torch.empty((48, cfg.R, 256), dtype=torch.uint8, device=dev)
-        scales = torch.empty((48, cfg.R), dtype=torch.float32, device=dev)
+    rb = eg.RECORD_BYTES if record else 256
+    kw = {"pin_memory": True} if cfg.host_tables else {"device": dev}
+    tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, **kw)
     sd.fill_tables(tables, base.seed)
-    sd.fill_scales(scales, base.seed)
+    scales = None
+    if record:
+        sd.fill_record_scales(tables, base.seed)
+    else:
+        scales = torch.empty((48, cfg.R), dtype=torch.float32, **kw)
+        sd.fill_scales(scales, base.seed)
     W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=dev)
     g = torch.empty(cfg.d, dtype=torch.bfloat16, device=dev)
     h = torch.empty((cfg.tq, cfg.d), dtype=torch.bfloat16, device=dev)
@@ -308,7 +312,9 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; tables e4m3 ~ quantised N(0,1), per-row fp32 scales U[0.5,2])",
         "config": {"workload": args.workload + (" (reduced)" if args.rows or args.tokens else ""), "V": cfg.V, "R": cfg.R, "n_seqs": cfg.n_seqs,
                    "tokens_per_step_per_gpu": cfg.t_all, "query_tokens_per_step_per_gpu": nq, "d_model": cfg.d,
-                   "table_bytes": cfg.table_bytes, "tables_in": "pinned host" if host else "HBM",
+                   "table_bytes": 48 * cfg.R * rb, "tables_in": "pinned host" if host else "HBM",
+                   "row_layout": ("272-byte records: 256 e4m3 codes + the row's fp32 scale" if record
+                                  else "256-byte rows + separate fp32 scale array"),
                    "token_ids": ("uniform" if cfg.zipf_s == 0 else f"Zipf({cfg.zipf_s})"),
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world} (replicated tables)"},
         "step_roofline": {"nominal_bytes_per_token": nominal_bytes_per_token(cfg.d), "achieved_GBps": round(step_gbs, 1),
@@ -542,6 +548,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large", choices=["tiny", "decode", "prefill", "large", "host"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layout", default="separate", choices=["record", "separate"],
+                    help="table rows that carry their scale (record) or a separate scale array")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -42,18 +42,24 @@ class engram_config(ctypes.Structure):
         ("d_model", ctypes.c_int32),
         ("rows", ctypes.c_int64),
         ("rms_eps", ctypes.c_float),
-        ("reserved", ctypes.c_uint32),
+        ("row_layout", ctypes.c_uint32),
         ("seeds", ctypes.c_uint64 * N_TABLES),
     ]
 
 
-def make_config(vocab, rows, d_model, seeds, rms_eps=1e-6):
-    """An engram_config: V (pad id), R rows per table, d_model, 48 hash seeds."""
+ROWS_SEPARATE = 0  # tables [48][R][256] + scales [48][R]
+ROWS_RECORD = 1  # tables [48][R][272]: 256 codes + fp32 scale at byte 256; no scales array
+RECORD_BYTES = 272
+
+
+def make_config(vocab, rows, d_model, seeds, rms_eps=1e-6, row_layout=ROWS_SEPARATE):
+    """An engram_config: V (pad id), R rows per table, d_model, 48 hash seeds, row layout."""
     c = engram_config()
     c.vocab = int(vocab)
     c.rows = int(rows)
     c.d_model = int(d_model)
     c.rms_eps = float(rms_eps)
+    c.row_layout = int(row_layout)
     seeds = [int(s) for s in seeds]
     if len(seeds) != N_TABLES:
         raise ValueError("need 48 seeds")
@@ -123,6 +129,8 @@ def _stream(stream):
 
 
 def _need(t, dtype, name, cuda=True):
+    if t is None and name in ("scales", "host_scales"):
+        return  # rows that carry their scale (ROWS_RECORD)
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -304,7 +312,7 @@ def engram_stage(cfg, host_tables, host_scales, unique, n_unique, capacity, stag
     """Copy the unique rows from pinned host tables into device staging buffers."""
     _need(host_tables, torch.uint8, "host_tables", cuda=False)
     _need(host_scales, torch.float32, "host_scales", cuda=False)
-    if not (host_tables.is_pinned() and host_scales.is_pinned()):
+    if not (host_tables.is_pinned() and (host_scales is None or host_scales.is_pinned())):
         raise ValueError("host tables and scales must be in pinned host memory")
     dev = unique.device
     if staged_rows is None:

@@ -125,7 +125,8 @@ enum IdxMode { IDX_I64 = 0, IDX_STAGED_I32 = 1, IDX_HASH = 2 };
 
 struct GatherParams {
     const uint8_t *rows;
-    const float *scales;
+    const float *scales;     // separate scales, or nullptr when each row carries its scale
+    int64_t row_stride;      // 256 (codes only) or 272 (codes + fp32 scale at byte 256)
     const void *idx;     // IDX_I64 / IDX_STAGED_I32
     int64_t n_query;
     int64_t R;           // rows per table (HBM) or staging capacity (staged)
@@ -133,8 +134,9 @@ struct GatherParams {
     HashParams hp;       // IDX_HASH
 };
 
+// 4 blocks of 256 threads per SM (at most 64 registers a thread).
 template <int kMode, bool kBf16Out>
-__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams P) {
+__global__ void __launch_bounds__(256, 4) gather_kernel(const __grid_constant__ GatherParams P) {
     __shared__ uint64_t s_seed[kTables];
     if (kMode == IDX_HASH) {
         if (threadIdx.x < kTables) s_seed[threadIdx.x] = P.hp.seeds[threadIdx.x];
@@ -170,8 +172,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
         if (!ok) raise_error(ENGRAM_ERANGE);
         const int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
         if (ok) {
-            off = flat * kRowBytes;
-            sc = __ldg(P.scales + flat);
+            off = flat * P.row_stride;
+            sc = P.scales ? __ldg(P.scales + flat) : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
         }
     }
     const int half = lane >> 4;
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(256) dedup_remap_kernel(const int64_t *__restr
 // row pairs in flight, and the grid strides over the unique list.
 
 __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ host_tables,
-                                                    const float *__restrict__ host_scales,
+                                                    const float *__restrict__ host_scales, int64_t host_stride,
                                                     const int64_t *__restrict__ unique,
                                                     const int64_t *__restrict__ n_unique, int64_t capacity,
                                                     uint8_t *__restrict__ staged, float *__restrict__ staged_scales) {
@@ -377,12 +379,16 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
         for (int k = 0; k < kPairs; ++k) {
             const int64_t u = u0 + 2 * k + half;
             flat[k] = u < U ? __ldg(unique + u) : -1;
-            v[k] = flat[k] >= 0 ? *reinterpret_cast<const uint4 *>(host_tables + flat[k] * kRowBytes + c16 * 16)
+            v[k] = flat[k] >= 0 ? *reinterpret_cast<const uint4 *>(host_tables + flat[k] * host_stride + c16 * 16)
                                 : make_uint4(0, 0, 0, 0);
         }
         float sc[kPairs];
 #pragma unroll
-        for (int k = 0; k < kPairs; ++k) sc[k] = (c16 == 0 && flat[k] >= 0) ? host_scales[flat[k]] : 0.f;
+        for (int k = 0; k < kPairs; ++k)
+            sc[k] = (c16 == 0 && flat[k] >= 0)
+                        ? (host_scales ? host_scales[flat[k]]
+                                       : *reinterpret_cast<const float *>(host_tables + flat[k] * host_stride + kRowBytes))
+                        : 0.f;
 #pragma unroll
         for (int k = 0; k < kPairs; ++k) {
             const int64_t u = u0 + 2 * k + half;
@@ -414,7 +420,16 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 engram_status check_config(const engram_config *cfg) {
     if (!cfg) return ENGRAM_EINVAL;
     if (cfg->vocab < 1 || cfg->rows < 1 || cfg->d_model < 0) return ENGRAM_EINVAL;
+    if (cfg->row_layout != ENGRAM_ROWS_SEPARATE && cfg->row_layout != ENGRAM_ROWS_RECORD) return ENGRAM_EINVAL;
     return ENGRAM_OK;
+}
+
+static bool records(const engram_config *cfg) { return cfg->row_layout == ENGRAM_ROWS_RECORD; }
+static int64_t row_stride(const engram_config *cfg) { return records(cfg) ? ENGRAM_RECORD_BYTES : kRowBytes; }
+// The scales argument as the kernels see it: nullptr when rows carry their scale.
+static const float *scales_arg(const engram_config *cfg, const float *scales) { return records(cfg) ? nullptr : scales; }
+static bool scales_ok(const engram_config *cfg, const float *scales) {
+    return records(cfg) || (scales && (reinterpret_cast<uintptr_t>(scales) % 4) == 0);
 }
 
 // With ENGRAM_DEBUG set in the environment, failed CUDA calls are reported on
@@ -458,12 +473,14 @@ static void fill_hash_params(HashParams &a, const engram_config *cfg, const int3
 }
 
 // mode: IDX_I64 / IDX_STAGED_I32 / IDX_HASH; out: fp32 mem or bf16 X.
-engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const float *scales, const void *idx,
-                            const HashParams *hp, int64_t n_query, int64_t R, void *out, cudaStream_t st) {
+engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const float *scales, int64_t stride,
+                            const void *idx, const HashParams *hp, int64_t n_query, int64_t R, void *out,
+                            cudaStream_t st) {
     GatherParams P;
     memset(&P, 0, sizeof(P));
     P.rows = rows;
     P.scales = scales;
+    P.row_stride = stride;
     P.idx = idx;
     P.n_query = n_query;
     P.R = R;
@@ -527,11 +544,11 @@ engram_status dedup_launch(const engram_config *cfg, const int64_t *idx, int64_t
     return launch_status();
 }
 
-engram_status stage_launch(const uint8_t *host_tables, const float *host_scales, const int64_t *unique,
-                           const int64_t *n_unique, int64_t capacity, uint8_t *staged, float *staged_scales,
-                           cudaStream_t st) {
+engram_status stage_launch(const uint8_t *host_tables, const float *host_scales, int64_t host_stride,
+                           const int64_t *unique, const int64_t *n_unique, int64_t capacity, uint8_t *staged,
+                           float *staged_scales, cudaStream_t st) {
     const int blocks = num_sms() * 8;
-    stage_kernel<<<blocks, 256, 0, st>>>(host_tables, host_scales, unique, n_unique, capacity, staged,
+    stage_kernel<<<blocks, 256, 0, st>>>(host_tables, host_scales, host_stride, unique, n_unique, capacity, staged,
                                          staged_scales);
     return launch_status();
 }
@@ -736,9 +753,10 @@ extern "C" engram_status engram_gather_reduce(const engram_config *cfg, const ui
                                               const int64_t *idx, int64_t n_query, float *mem, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0) return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
-    if (!tables || !scales || !idx || !mem) return ENGRAM_EINVAL;
-    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(idx, 8) || !aligned(mem, 16)) return ENGRAM_EINVAL;
-    return gather_launch(IDX_I64, false, tables, scales, idx, nullptr, n_query, cfg->rows, mem, (cudaStream_t)stream);
+    if (!tables || !scales_ok(cfg, scales) || !idx || !mem) return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(idx, 8) || !aligned(mem, 16)) return ENGRAM_EINVAL;
+    return gather_launch(IDX_I64, false, tables, scales_arg(cfg, scales), row_stride(cfg), idx, nullptr, n_query,
+                         cfg->rows, mem, (cudaStream_t)stream);
 }
 
 extern "C" size_t engram_dedup_workspace_bytes(const engram_config *cfg) {
@@ -761,10 +779,11 @@ extern "C" engram_status engram_stage(const engram_config *cfg, const uint8_t *h
                                       const int64_t *unique, const int64_t *n_unique, int64_t capacity,
                                       uint8_t *staged_rows, float *staged_scales, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || capacity < 1) return ENGRAM_EINVAL;
-    if (!host_tables || !host_scales || !unique || !n_unique || !staged_rows || !staged_scales) return ENGRAM_EINVAL;
-    if (!aligned(host_tables, 16) || !aligned(staged_rows, 16) || !aligned(host_scales, 4)) return ENGRAM_EINVAL;
-    return stage_launch(host_tables, host_scales, unique, n_unique, capacity, staged_rows, staged_scales,
-                        (cudaStream_t)stream);
+    if (!host_tables || !scales_ok(cfg, host_scales) || !unique || !n_unique || !staged_rows || !staged_scales)
+        return ENGRAM_EINVAL;
+    if (!aligned(host_tables, 16) || !aligned(staged_rows, 16)) return ENGRAM_EINVAL;
+    return stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), unique, n_unique, capacity,
+                        staged_rows, staged_scales, (cudaStream_t)stream);
 }
 
 extern "C" engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_t *staged_rows,
@@ -774,8 +793,8 @@ extern "C" engram_status engram_gather_reduce_staged(const engram_config *cfg, c
     if (n_query == 0) return ENGRAM_OK;
     if (!staged_rows || !staged_scales || !idx_staged || !mem) return ENGRAM_EINVAL;
     if (!aligned(staged_rows, 16) || !aligned(mem, 16) || !aligned(idx_staged, 4)) return ENGRAM_EINVAL;
-    return gather_launch(IDX_STAGED_I32, false, staged_rows, staged_scales, idx_staged, nullptr, n_query, capacity, mem,
-                         (cudaStream_t)stream);
+    return gather_launch(IDX_STAGED_I32, false, staged_rows, staged_scales, kRowBytes, idx_staged, nullptr, n_query,
+                         capacity, mem, (cudaStream_t)stream);
 }
 
 extern "C" engram_status engram_fuse(const engram_config *cfg, const float *mem, const uint16_t *W_out,
@@ -798,11 +817,11 @@ extern "C" engram_status engram_forward(const engram_config *cfg, const int32_t 
                                         void *workspace, size_t workspace_bytes, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
-    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales || !workspace) return ENGRAM_EINVAL;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales_ok(cfg, scales) || !workspace)
+        return ENGRAM_EINVAL;
     if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
     if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
-    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(workspace, 256) || !aligned(tokens, 4) ||
-        !aligned(seq_offsets, 8))
+    if (!aligned(tables, 16) || !aligned(workspace, 256) || !aligned(tokens, 4) || !aligned(seq_offsets, 8))
         return ENGRAM_EINVAL;
     if (n_query > (INT64_C(1) << 31)) return ENGRAM_EINVAL;
     if (workspace_bytes < forward_bytes(n_query)) return ENGRAM_ENOMEM;
@@ -810,7 +829,8 @@ extern "C" engram_status engram_forward(const engram_config *cfg, const int32_t 
     uint16_t *X = static_cast<uint16_t *>(workspace);
     HashParams hp;
     fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
-    engram_status s = gather_launch(IDX_HASH, true, tables, scales, nullptr, &hp, n_query, cfg->rows, X, st);
+    engram_status s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), nullptr, &hp,
+                                    n_query, cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
 }
@@ -820,15 +840,15 @@ extern "C" engram_status engram_gather_x(const engram_config *cfg, const int32_t
                                          const float *scales, uint16_t *X, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
-    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales || !X) return ENGRAM_EINVAL;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales_ok(cfg, scales) || !X) return ENGRAM_EINVAL;
     if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
-    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(X, 16) || !aligned(tokens, 4) ||
-        !aligned(seq_offsets, 8))
+    if (!aligned(tables, 16) || !aligned(X, 16) || !aligned(tokens, 4) || !aligned(seq_offsets, 8))
         return ENGRAM_EINVAL;
     if (n_query > (INT64_C(1) << 40)) return ENGRAM_EINVAL;
     HashParams hp;
     fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
-    return gather_launch(IDX_HASH, true, tables, scales, nullptr, &hp, n_query, cfg->rows, X, (cudaStream_t)stream);
+    return gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), nullptr, &hp, n_query,
+                         cfg->rows, X, (cudaStream_t)stream);
 }
 
 extern "C" engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const uint16_t *W_out,
@@ -860,13 +880,12 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0 || capacity < 1)
         return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
-    if (!tokens || !seq_offsets || n_seqs < 1 || !host_tables || !host_scales || !workspace || !n_unique ||
-        !ev_dedup || !ev_staged)
+    if (!tokens || !seq_offsets || n_seqs < 1 || !host_tables || !scales_ok(cfg, host_scales) || !workspace ||
+        !n_unique || !ev_dedup || !ev_staged)
         return ENGRAM_EINVAL;
     if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
     if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
-    if (!aligned(host_tables, 16) || !aligned(host_scales, 4) || !aligned(workspace, 256) || !aligned(n_unique, 8))
-        return ENGRAM_EINVAL;
+    if (!aligned(host_tables, 16) || !aligned(workspace, 256) || !aligned(n_unique, 8)) return ENGRAM_EINVAL;
     if (n_query * kTables >= (INT64_C(1) << 31) || capacity >= (INT64_C(1) << 31)) return ENGRAM_EINVAL;
     if (workspace_bytes < engram_forward_host_workspace_bytes(cfg, n_query, capacity)) return ENGRAM_ENOMEM;
     cudaStream_t st = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
@@ -891,11 +910,12 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
     if (s != ENGRAM_OK) return s;
     if (cudaEventRecord((cudaEvent_t)ev_dedup, st) != cudaSuccess) return ENGRAM_ECUDA;
     if (cudaStreamWaitEvent(side, (cudaEvent_t)ev_dedup, 0) != cudaSuccess) return ENGRAM_ECUDA;
-    s = stage_launch(host_tables, host_scales, unique, n_unique, capacity, rows, sc, side);
+    s = stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), unique, n_unique, capacity, rows, sc,
+                     side);
     if (s != ENGRAM_OK) return s;
     if (cudaEventRecord((cudaEvent_t)ev_staged, side) != cudaSuccess) return ENGRAM_ECUDA;
     if (cudaStreamWaitEvent(st, (cudaEvent_t)ev_staged, 0) != cudaSuccess) return ENGRAM_ECUDA;
-    s = gather_launch(IDX_STAGED_I32, true, rows, sc, idx_staged, nullptr, n_query, capacity, X, st);
+    s = gather_launch(IDX_STAGED_I32, true, rows, sc, kRowBytes, idx_staged, nullptr, n_query, capacity, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
 }
@@ -938,11 +958,10 @@ extern "C" engram_status engram_forward_no_workspace(const engram_config *cfg, c
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
     if (n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY) return ENGRAM_ENOMEM;  // past the built-in scratch
-    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales) return ENGRAM_EINVAL;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales_ok(cfg, scales)) return ENGRAM_EINVAL;
     if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
     if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
-    if (!aligned(tables, 16) || !aligned(scales, 4) || !aligned(tokens, 4) || !aligned(seq_offsets, 8))
-        return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(tokens, 4) || !aligned(seq_offsets, 8)) return ENGRAM_EINVAL;
     uint16_t *X = nullptr;
     engram_status s = no_workspace_scratch(&X);
     if (s != ENGRAM_OK) return s;
@@ -952,7 +971,8 @@ extern "C" engram_status engram_forward_no_workspace(const engram_config *cfg, c
     // X rows [0, n_query) are all written before the projection reads them,
     // and the projection's tensor map stops at n_query rows: nothing left in
     // the array by an earlier call is read, so nothing needs clearing.
-    s = gather_launch(IDX_HASH, true, tables, scales, nullptr, &hp, n_query, cfg->rows, X, st);
+    s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), nullptr, &hp, n_query,
+                      cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
 }

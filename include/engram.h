@@ -62,12 +62,25 @@ typedef enum {
 #define ENGRAM_ROW_BYTES 256
 #define ENGRAM_MEM_DIM 512
 
+/* Table row layouts (engram_config.row_layout):
+ *  ENGRAM_ROWS_SEPARATE: tables e4m3 [48][R][256]; scales fp32 [48][R] in their
+ *                        own array (the `scales` argument).
+ *  ENGRAM_ROWS_RECORD:   tables [48][R][272]: bytes 0..255 the row's e4m3 codes,
+ *                        256..259 its fp32 scale, 260..271 padding; the
+ *                        `scales` argument is ignored (may be NULL).  One
+ *                        contiguous read per row instead of two scattered ones
+ *                        (the pages describe a row as 256 B of FP8 plus its
+ *                        scales, "Engram: the table that is never multiplied"). */
+#define ENGRAM_ROWS_SEPARATE 0
+#define ENGRAM_ROWS_RECORD 1
+#define ENGRAM_RECORD_BYTES 272
+
 typedef struct {
-    int32_t vocab;   /* V: token ids must lie in [0, V); V itself is the pad id */
-    int32_t d_model; /* d: residual width; engram_fuse needs d % 256 == 0 */
-    int64_t rows;    /* R: rows per table, R >= 1, 48*R*256 bytes of table */
-    float rms_eps;   /* eps inside the rmsnorm of the gate (1e-6 by default) */
-    uint32_t reserved;
+    int32_t vocab;       /* V: token ids must lie in [0, V); V itself is the pad id */
+    int32_t d_model;     /* d: residual width; engram_fuse needs d % 256 == 0 */
+    int64_t rows;        /* R: rows per table, R >= 1 */
+    float rms_eps;       /* eps inside the rmsnorm of the gate (1e-6 by default) */
+    uint32_t row_layout; /* ENGRAM_ROWS_SEPARATE or ENGRAM_ROWS_RECORD */
     uint64_t seeds[ENGRAM_N_TABLES]; /* hash seed of table j */
 } engram_config;
 
@@ -98,8 +111,8 @@ engram_status engram_hash(const engram_config *cfg, const int32_t *tokens, const
 
 /*
  * Step 3 (gather, dequantise, per-module sum).
- *   tables int8 e4m3 codes [48][R][256], 16-byte aligned
- *   scales fp32 [48][R]
+ *   tables e4m3 codes [48][R][256] (or [48][R][272] records), 16-byte aligned
+ *   scales fp32 [48][R] (ENGRAM_ROWS_SEPARATE only)
  *   idx    int64 [n_query][48], each in [0, R) (out-of-range rows read nothing
  *          and set ENGRAM_ERANGE)
  *   mem    fp32 [n_query][512] output, module 0 then module 1, 16-byte aligned
@@ -198,8 +211,10 @@ engram_status engram_dedup(const engram_config *cfg, const int64_t *idx, int64_t
 /*
  * engram_stage: copy the U = min(*n_unique, capacity) unique rows and their
  * scales from host tables into device staging buffers.
- *   host_tables e4m3 [48][R][256] in pinned host memory (16-byte aligned)
- *   host_scales fp32 [48][R] in pinned host memory
+ *   host_tables e4m3 [48][R][256] (or [48][R][272] records) in pinned host
+ *               memory (16-byte aligned)
+ *   host_scales fp32 [48][R] in pinned host memory (ENGRAM_ROWS_SEPARATE only)
+ *   The staging buffers are always 256-byte rows plus a separate scale array.
  *   staged_rows [capacity][256] and staged_scales [capacity] (device)
  * Enqueued on `stream` (normally a side stream that waited for the dedup).
  */

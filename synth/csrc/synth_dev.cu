@@ -48,9 +48,10 @@ __device__ __forceinline__ uint32_t word_of(const uint64_t out[4], int i) {
     return (uint32_t)(out[i >> 1] >> (32 * (i & 1)));
 }
 
-// e4m3 codes: table j0+jj, row r, code c <- u32 word r*256 + c of stream (seed, 0x100 + j)
-__global__ void fill_tables_kernel(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, const uint32_t *thr_g,
-                                   const uint16_t *codes_g, int n_codes) {
+// e4m3 codes: table j0+jj, row r, code c <- u32 word r*256 + c of stream (seed, 0x100 + j);
+// rows are row_stride bytes apart (256, or 272 for rows that carry their scale)
+__global__ void fill_tables_kernel(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, int64_t row_stride,
+                                   const uint32_t *thr_g, const uint16_t *codes_g, int n_codes) {
     extern __shared__ uint32_t sm[];
     uint32_t *thr = sm;
     uint16_t *codes = reinterpret_cast<uint16_t *>(sm + n_codes);
@@ -72,12 +73,14 @@ __global__ void fill_tables_kernel(uint8_t *dst, uint64_t seed, int j0, int nj, 
             const uint32_t code = codes[cdf_index(thr, n_codes - 1, word_of(out, k))] & 0xFFu;
             if (k < 4) lo |= code << (8 * k); else hi |= code << (8 * (k - 4));
         }
-        *reinterpret_cast<uint2 *>(dst + ((int64_t)jj * R + (int64_t)row) * 256 + b * 8) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2 *>(dst + ((int64_t)jj * R + (int64_t)row) * row_stride + b * 8) = make_uint2(lo, hi);
     }
 }
 
-// per-row scales of tables j0.. : word = row of stream (seed, 0x200 + j)
-__global__ void fill_scales_kernel(float *dst, uint64_t seed, int j0, int nj, int64_t R) {
+// per-row scales of tables j0.. : word = row of stream (seed, 0x200 + j); the
+// scale of row (jj, row) goes to dst + (jj*R + row)*stride + offset bytes
+__global__ void fill_scales_kernel(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, int64_t stride,
+                                   int64_t offset) {
     const int64_t blocks_per_table = (R + 7) / 8;
     const int64_t total = (int64_t)nj * blocks_per_table;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -91,7 +94,8 @@ __global__ void fill_scales_kernel(float *dst, uint64_t seed, int j0, int nj, in
             if (row < R) {
                 const uint32_t u = word_of(out, k);
                 const long long x = (1ll << 24) + 3ll * (long long)(u >> 8);
-                dst[jj * R + row] = __ll2float_rn(x) * 0x1p-25f;  // exact power-of-two scaling
+                *reinterpret_cast<float *>(dst + (jj * R + row) * stride + offset) =
+                    __ll2float_rn(x) * 0x1p-25f;  // exact power-of-two scaling
             }
         }
     }
@@ -134,16 +138,19 @@ int grid_for(int64_t work) {
 
 }  // namespace
 
-extern "C" int synth_fill_tables(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, const uint32_t *thr,
-                                 const uint16_t *codes, int n_codes, void *stream) {
+extern "C" int synth_fill_tables(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, int64_t row_stride,
+                                 const uint32_t *thr, const uint16_t *codes, int n_codes, void *stream) {
     const size_t sm = (size_t)n_codes * 4 + (size_t)n_codes * 2;
-    fill_tables_kernel<<<grid_for((int64_t)nj * R * 32), 256, sm, (cudaStream_t)stream>>>(dst, seed, j0, nj, R, thr,
-                                                                                        codes, n_codes);
+    fill_tables_kernel<<<grid_for((int64_t)nj * R * 32), 256, sm, (cudaStream_t)stream>>>(dst, seed, j0, nj, R,
+                                                                                        row_stride, thr, codes,
+                                                                                        n_codes);
     return (int)cudaGetLastError();
 }
 
-extern "C" int synth_fill_scales(float *dst, uint64_t seed, int j0, int nj, int64_t R, void *stream) {
-    fill_scales_kernel<<<grid_for((int64_t)nj * ((R + 7) / 8)), 256, 0, (cudaStream_t)stream>>>(dst, seed, j0, nj, R);
+extern "C" int synth_fill_scales(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, int64_t stride,
+                                 int64_t offset, void *stream) {
+    fill_scales_kernel<<<grid_for((int64_t)nj * ((R + 7) / 8)), 256, 0, (cudaStream_t)stream>>>(dst, seed, j0, nj, R,
+                                                                                            stride, offset);
     return (int)cudaGetLastError();
 }
 

@@ -42,8 +42,8 @@ def _load():
             raise RuntimeError(f"{_LIB} is not built; run __graft_entry__.build()")
         lib = ctypes.CDLL(_LIB)
         P, i64, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
-        lib.synth_fill_tables.argtypes = [P, u64, i32, i32, i64, P, P, i32, P]
-        lib.synth_fill_scales.argtypes = [P, u64, i32, i32, i64, P]
+        lib.synth_fill_tables.argtypes = [P, u64, i32, i32, i64, i64, P, P, i32, P]
+        lib.synth_fill_scales.argtypes = [P, u64, i32, i32, i64, i64, i64, P]
         lib.synth_fill_bf16.argtypes = [P, u64, u64, u64, i64, P, P, i32, P]
         for f in (lib.synth_fill_tables, lib.synth_fill_scales, lib.synth_fill_bf16):
             f.restype = ctypes.c_int
@@ -73,20 +73,32 @@ def _check(rc):
         raise RuntimeError(f"synth kernel launch failed: cudaError {rc}")
 
 
+RECORD_BYTES = 272  # 256 e4m3 codes + fp32 scale at byte 256 + padding
+
+
 def fill_tables(dst, seed, j0=0):
-    """dst uint8 [nj, R, 256] (CUDA or pinned CPU tensor): tables j0..j0+nj-1."""
+    """dst uint8 [nj, R, 256] or [nj, R, 272] (rows that carry their scale;
+    call fill_record_scales too) -- CUDA or pinned CPU tensor."""
     nj, R, rb = dst.shape
-    assert rb == ROW_BYTES and dst.dtype == torch.uint8 and dst.is_contiguous() and j0 + nj <= N_TABLES
+    assert rb in (ROW_BYTES, RECORD_BYTES) and dst.dtype == torch.uint8 and dst.is_contiguous() and j0 + nj <= N_TABLES
     thr, codes, n = _cdf_on_device("e4m3", 1.0, "cuda")
-    _check(_load().synth_fill_tables(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, ctypes.c_void_p(thr.data_ptr()),
-                                     ctypes.c_void_p(codes.data_ptr()), n, _stream()))
+    _check(_load().synth_fill_tables(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, rb,
+                                     ctypes.c_void_p(thr.data_ptr()), ctypes.c_void_p(codes.data_ptr()), n, _stream()))
 
 
 def fill_scales(dst, seed, j0=0):
     """dst float32 [nj, R]."""
     nj, R = dst.shape
     assert dst.dtype == torch.float32 and dst.is_contiguous()
-    _check(_load().synth_fill_scales(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, _stream()))
+    _check(_load().synth_fill_scales(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, 4, 0, _stream()))
+
+
+def fill_record_scales(dst, seed, j0=0):
+    """The fp32 scales into bytes 256..259 of each 272-byte row of dst."""
+    nj, R, rb = dst.shape
+    assert rb == RECORD_BYTES and dst.dtype == torch.uint8 and dst.is_contiguous()
+    _check(_load().synth_fill_scales(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, RECORD_BYTES, ROW_BYTES,
+                                     _stream()))
 
 
 def fill_bf16(dst, seed, stream, sigma, word0=0):

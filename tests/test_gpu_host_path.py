@@ -94,6 +94,19 @@ def test_host_path_bit_identical_to_hbm_path(eg):
     check_h(h_host[torch.from_numpy(q).cuda()], ref_h)
 
 
+def test_host_path_record_layout(eg):
+    """Host tables as 272-byte records (scale inside the row): same h bits as
+    the HBM path with separate scales."""
+    a = Workload(SMALL_HOST)
+    b = Workload(SMALL_HOST, host_tables=True, layout="record")
+    ha, hb = a.fresh_h(), b.fresh_h()
+    eg.engram_forward(a.c, a.tokens, a.seq_offsets, a.tables, a.scales, a.W, a.g, ha)
+    eg.engram_forward_host(b.c, b.tokens, b.seq_offsets, b.tables, None, b.W, b.g, hb, capacity=b.cfg.tq * 48)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(ha.view(torch.int16), hb.view(torch.int16))
+
+
 def test_host_path_full_size(eg):
     """The host-table workload at full size (51.5 GB of pinned tables)."""
     cfg = CONFIGS["host"]

@@ -111,6 +111,29 @@ def test_split_halves_equal_forward(eg, name):
     assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged_prime", "prefill_small", "decode_small"])
+def test_record_layout_same_bits(eg, name):
+    """Rows that carry their scale (272-byte records) give the same mem, X and
+    h bits as the separate-scales layout, and match the oracle."""
+    a = Workload(SMALL[name])
+    b = Workload(SMALL[name], layout="record")
+    assert torch.equal(b.tables[:, :, :256], a.tables)
+    assert torch.equal(b.tables[:, :, 256:260].contiguous().view(torch.float32).squeeze(-1), a.scales)
+    ia = eg.engram_hash(a.c, a.tokens, a.seq_offsets, last_n=a.cfg.last_n)
+    ma = eg.engram_gather_reduce(a.c, a.tables, a.scales, ia)
+    mb = eg.engram_gather_reduce(b.c, b.tables, None, ia)
+    ha, hb = a.fresh_h(), b.fresh_h()
+    eg.engram_forward(a.c, a.tokens, a.seq_offsets, a.tables, a.scales, a.W, a.g, ha, last_n=a.cfg.last_n)
+    eg.engram_forward(b.c, b.tokens, b.seq_offsets, b.tables, None, b.W, b.g, hb, last_n=b.cfg.last_n)
+    _clear(eg)
+    assert torch.equal(ma, mb)
+    assert torch.equal(ha.view(torch.int16), hb.view(torch.int16))
+    q = np.arange(a.cfg.tq)
+    _, rmem, bound, rh, _ = a.ref_for(q)
+    check_mem(mb.cpu().numpy(), rmem, bound)
+    check_h(hb, rh)
+
+
 def test_generator_twin_rows_match_host(eg):
     """The device-filled tables/scales/h equal the host draws bit for bit."""
     cfg = SMALL["ragged_prime"]

@@ -18,27 +18,36 @@ MEM_TOL = 1e-5  # |gpu - ref| <= MEM_TOL * sum_j |term_j| on the module sums
 
 
 class Workload:
-    def __init__(self, cfg, device="cuda", tables=True, host_tables=False):
+    """layout "separate": tables [48,R,256] + scales [48,R];
+    layout "record": tables [48,R,272] with each row's fp32 scale at byte 256 (scales None)."""
+
+    def __init__(self, cfg, device="cuda", tables=True, host_tables=False, layout="separate"):
         import engram_gram_hash_gb300 as eg
 
         self.cfg = cfg
         self.dev = torch.device(device)
         self.seeds = default_seeds()
-        self.c = eg.make_config(cfg.V, cfg.R, cfg.d, self.seeds, cfg.rms_eps)
+        self.layout = layout
+        rl = eg.ROWS_RECORD if layout == "record" else eg.ROWS_SEPARATE
+        self.c = eg.make_config(cfg.V, cfg.R, cfg.d, self.seeds, cfg.rms_eps, row_layout=rl)
         self.tok, self.offs = make_tokens(cfg)
         self.qpos = query_positions(cfg, self.offs)
         self.tokens = torch.from_numpy(self.tok).to(self.dev)
         self.seq_offsets = torch.from_numpy(self.offs).to(self.dev)
         self.tables = self.scales = None
         if tables:
+            rb = 272 if layout == "record" else 256
             if host_tables:
-                self.tables = torch.empty((48, cfg.R, 256), dtype=torch.uint8, pin_memory=True)
-                self.scales = torch.empty((48, cfg.R), dtype=torch.float32, pin_memory=True)
+                self.tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, pin_memory=True)
             else:
-                self.tables = torch.empty((48, cfg.R, 256), dtype=torch.uint8, device=self.dev)
-                self.scales = torch.empty((48, cfg.R), dtype=torch.float32, device=self.dev)
+                self.tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, device=self.dev)
             sd.fill_tables(self.tables, cfg.seed)
-            sd.fill_scales(self.scales, cfg.seed)
+            if layout == "record":
+                sd.fill_record_scales(self.tables, cfg.seed)
+            else:
+                kw = {"pin_memory": True} if host_tables else {"device": self.dev}
+                self.scales = torch.empty((48, cfg.R), dtype=torch.float32, **kw)
+                sd.fill_scales(self.scales, cfg.seed)
         self.W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=self.dev)
         self.g = torch.empty(cfg.d, dtype=torch.bfloat16, device=self.dev)
         sd.fill_w_out(self.W, cfg.seed)
