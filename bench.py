@@ -73,7 +73,7 @@ def kernel_source_hash():
 def ncu_traffic(kernel, workload, units):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
     if there is none for the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")  # JSON text
     if not os.path.exists(p):
         return None
     with open(p) as f:
