@@ -167,6 +167,28 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sel), "window": window}
 
 
+# ------------------------------------------------------ multi-rank pieces ----
+
+
+def rank_config(base, rank):
+    """Rank r's workload under weak scaling: the same tables (the model's
+    weights, replicated), its own token batch and residual (seed + 1000 r)."""
+    return base if rank == 0 else base.with_(seed=base.seed + 1000 * rank)
+
+
+def job_rate(local_ms, steps, units_per_rank, world, device):
+    """Whole-job throughput: every rank's units over the slowest rank's time.
+    Returns (units per second, max ms over ranks)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return units_per_rank * world / (ms_max * 1e-3 / steps), ms_max
+
+
 # --------------------------------------------------------------- our arm ----
 
 
@@ -187,7 +209,7 @@ def run_ours(args, rank, world, local_rank):
     if args.tokens:
         base = base.with_(seq_lens=tuple(min(L, args.tokens) for L in base.seq_lens))
     # weak scaling: rank r draws its own token batch (tables are replicated weights)
-    cfg = base.with_(seed=base.seed) if rank == 0 else base.with_(seed=base.seed + 1000 * rank)
+    cfg = rank_config(base, rank)
     seeds = default_seeds()
     record = args.layout == "record"
     c = eg.make_config(cfg.V, cfg.R, cfg.d, seeds, cfg.rms_eps,
@@ -271,10 +293,7 @@ def run_ours(args, rank, world, local_rank):
     status = eg.engram_last_error()
     if status != 0:
         raise RuntimeError(f"device error {status} in the timed region")
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    value, ms_max = job_rate(ms, K, cfg.tq, world, dev)
     clocks = cs.summary()
 
     peaks = measured_peaks()
@@ -302,8 +321,6 @@ def run_ours(args, rank, world, local_rank):
     if host:
         roofline = host_link_roofline(eg, c, cfg, tokens, seq_offsets, tables, scales, nq, dev)
 
-    tokens_total = nq * world
-    value = tokens_total / (ms_max * 1e-3 / K)
     step_gbs = nominal_bytes_per_token(cfg.d) * nq / (ms_max * 1e-3 / K) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -417,14 +434,10 @@ def e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h_dev,
         one()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    rate, ms = job_rate(a.elapsed_time(b), K, nq, world, dev)
     h2d = tok_h.numel() * 4 + off_h.numel() * 8 + h_in.numel() * 2
     d2h = h_out.numel() * 2
-    return {"value": round(nq * world / (ms * 1e-3 / K), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    return {"value": round(rate, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / K, 4), "api": "engram_forward"}
 
 
