@@ -18,7 +18,6 @@
 
 #include "common.cuh"
 #include "fuse.cuh"
-#include "fuse6.cuh"
 
 namespace engram {
 
@@ -666,100 +665,6 @@ static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &x
     return ENGRAM_EINVAL;
 }
 
-// fuse6 (X in TMEM): CTAs per cluster for n128 128-column chunks; a slice
-// must be 2, 4, 8 or 16 chunks.  Many tiles: 8 chunks (1024 columns) per
-// CTA; few tiles: as many CTAs as fit.  0 if d has no valid split.
-static int pick_groups6(int64_t m_tiles, int n128) {
-    const int sms = num_sms();
-    int best = 0;
-    double best_score = 1e30;
-    for (int g = 1; g <= fuse6::MAX_GROUPS; ++g) {
-        if (n128 % g) continue;
-        const int nch = n128 / g;
-        if (nch != 2 && nch != 4 && nch != 8 && nch != 16) continue;
-        double score;
-        if (m_tiles * 2 >= sms)
-            score = fabs(log2((double)nch) - 3.0) * 100.0 + g;
-        else
-            score = (m_tiles * g <= sms ? 0.0 : 1000.0) - g;
-        if (score < best_score) {
-            best_score = score;
-            best = g;
-        }
-    }
-    return best;
-}
-
-template <int NCH>
-static engram_status fuse6_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse6::Params &p,
-                                    cudaStream_t st) {
-    auto kern = fuse6::fuse6_kernel<NCH>;
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fuse6::SMEM_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fuse6 smem)");
-        attr_done[dev] = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.groups;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(fuse6::NUM_THREADS);
-    cfg.dynamicSmemBytes = fuse6::SMEM_BYTES;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int max_clusters[64][fuse6::MAX_GROUPS + 1] = {};
-    int &mc = max_clusters[dev][p.groups];
-    if (mc == 0) {
-        cfg.gridDim = dim3(p.groups * 64);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-            cudaGetLastError();
-            n = num_sms() / p.groups;
-        }
-        mc = n;
-    }
-    const int64_t clusters = std::min<int64_t>(p.m_tiles, mc);
-    cfg.gridDim = dim3((unsigned)(clusters * p.groups));
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, wmap, xmap, p);
-    if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(fuse6)");
-    return launch_status();
-}
-
-// y = X @ W_out and the gated residual update from bf16 X, X held in TMEM.
-static engram_status fuse6_launch(const engram_config *cfg, const uint16_t *x_bf16, const uint16_t *W,
-                                  const uint16_t *g, uint16_t *h, int64_t n_query, cudaStream_t st) {
-    const int d = cfg->d_model;
-    const int n128 = d / fuse6::BN;
-    fuse6::Params p;
-    p.g = g;
-    p.h = h;
-    p.n_query = n_query;
-    p.m_tiles = (n_query + fuse6::BM - 1) / fuse6::BM;
-    p.d = d;
-    p.groups = pick_groups6(p.m_tiles, n128);
-    if (p.groups == 0) return ENGRAM_EINVAL;
-    p.nch = n128 / p.groups;
-    p.eps = cfg->rms_eps;
-    p.inv_sqrt_d = 1.0f / sqrtf((float)d);
-    CUtensorMap wmap, xmap;
-    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, fuse6::BK)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
-    if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse6::BK, fuse6::BM))
-        return cuda_fail(cudaErrorInvalidValue, "X tensor map");
-    switch (p.nch) {
-        case 2: return fuse6_launch_t<2>(wmap, xmap, p, st);
-        case 4: return fuse6_launch_t<4>(wmap, xmap, p, st);
-        case 8: return fuse6_launch_t<8>(wmap, xmap, p, st);
-        case 16: return fuse6_launch_t<16>(wmap, xmap, p, st);
-    }
-    return ENGRAM_EINVAL;
-}
-
 // y = X @ W_out and the gated residual update.  X comes either from fp32 mem
 // (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
 engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint16_t *x_bf16, const uint16_t *W,
@@ -782,7 +687,11 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     CUtensorMap wmap, xmap;
     memset(&xmap, 0, sizeof(xmap));
     if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, fuse::BK)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
-    if (x_bf16) return fuse6_launch(cfg, x_bf16, W, g, h, n_query, st);
+    if (x_bf16) {
+        if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
+            return cuda_fail(cudaErrorInvalidValue, "X tensor map");
+        return fuse_dispatch<fuse::X_FROM_BF16_TMA>(wmap, xmap, p, st);
+    }
     return fuse_dispatch<fuse::X_FROM_F32_MEM>(wmap, xmap, p, st);
 }
 
