@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(256) dedup_remap_kernel(const int64_t *__restr
 
 // ==================================================================== stage ==
 // Copy unique rows (and their scales) from host tables into device staging.
-// Each half-warp moves one 256-byte row with 16-byte loads; a warp keeps four
+// Each half-warp moves one 256-byte row with 16-byte loads; a warp keeps eight
 // row pairs in flight, and the grid strides over the unique list.
 
 __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ host_tables,
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
     const int half = lane >> 4, c16 = lane & 15;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    constexpr int kPairs = 4;
+    constexpr int kPairs = 8;
     for (int64_t u0 = warp * 2 * kPairs; u0 < U; u0 += n_warps * 2 * kPairs) {
         uint4 v[kPairs];
         int64_t flat[kPairs];
