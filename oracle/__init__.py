@@ -56,6 +56,10 @@ def _load():
         lib.orc_gather_reduce_rows.argtypes = [P, P, i64, P]
         lib.orc_gather_reduce.restype = ctypes.c_int
         lib.orc_gather_reduce.argtypes = [P, P, i64, P, i64, P]
+        lib.orc_e8m0_value.restype = ctypes.c_double
+        lib.orc_e8m0_value.argtypes = [ctypes.c_uint8]
+        lib.orc_gather_reduce_mx_rows.restype = None
+        lib.orc_gather_reduce_mx_rows.argtypes = [P, P, i64, P]
         lib.orc_bf16_value.restype = ctypes.c_double
         lib.orc_bf16_value.argtypes = [ctypes.c_uint16]
         lib.orc_bf16_rne.restype = ctypes.c_uint16
@@ -125,6 +129,21 @@ def gather_reduce_rows(rows, scales):
     assert rows.shape == (T, N_TABLES, ROW) and scales.shape == (T, N_TABLES)
     mem = np.zeros((T, MEM), dtype=np.float64)
     _load().orc_gather_reduce_rows(_p(rows), _p(scales), T, _p(mem))
+    return mem
+
+
+def e8m0_value(code):
+    return _load().orc_e8m0_value(int(code))
+
+
+def gather_reduce_mx_rows(rows, escales):
+    """mem float64 [T,512] from MX rows: codes uint8 [T,48,256], E8M0 block scales uint8 [T,48,8]."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint8)
+    escales = np.ascontiguousarray(escales, dtype=np.uint8)
+    T = rows.shape[0]
+    assert rows.shape == (T, N_TABLES, ROW) and escales.shape == (T, N_TABLES, 8)
+    mem = np.zeros((T, MEM), dtype=np.float64)
+    _load().orc_gather_reduce_mx_rows(_p(rows), _p(escales), T, _p(mem))
     return mem
 
 

@@ -150,6 +150,37 @@ static void reduce_token(const uint8_t *const *rows, const float *scale48, doubl
     }
 }
 
+/* OCP MX E8M0 scale byte: 2^(E - 127); E = 255 is NaN. */
+double orc_e8m0_value(uint8_t e) {
+    if (e == 255) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* MXFP8-style rows (256 bytes of FP8 plus 8 bytes of scales per row,
+ * "Engram: the table that is never multiplied"): code c of table j's row is
+ * scaled by the E8M0 scale of its 32-code block, escale[j][c / 32].
+ * mem[256*m + c] = sum over the module's 24 tables, ascending j. */
+static void reduce_token_mx(const uint8_t *const *rows, const uint8_t *const *esc, double *mem512) {
+    for (int k = 0; k < ORC_MEM; ++k) mem512[k] = 0.0;
+    for (int j = 0; j < ORC_TABLES; ++j) {
+        int m = table_module(j);
+        for (int c = 0; c < ORC_ROW; ++c)
+            mem512[ORC_ROW * m + c] += orc_e8m0_value(esc[j][c / 32]) * orc_e4m3_value(rows[j][c]);
+    }
+}
+
+/* MX rows given explicitly: rows [T][48][256] codes, escales [T][48][8]. */
+void orc_gather_reduce_mx_rows(const uint8_t *rows, const uint8_t *escales, int64_t T, double *mem) {
+    for (int64_t t = 0; t < T; ++t) {
+        const uint8_t *ptr[ORC_TABLES], *esc[ORC_TABLES];
+        for (int j = 0; j < ORC_TABLES; ++j) {
+            ptr[j] = rows + (t * ORC_TABLES + j) * ORC_ROW;
+            esc[j] = escales + (t * ORC_TABLES + j) * 8;
+        }
+        reduce_token_mx(ptr, esc, mem + t * ORC_MEM);
+    }
+}
+
 /* Gather from explicit rows: rows [T][48][256] bytes, scales [T][48]. */
 void orc_gather_reduce_rows(const uint8_t *rows, const float *scales, int64_t T, double *mem) {
     for (int64_t t = 0; t < T; ++t) {

@@ -313,6 +313,50 @@ def test_gather_rows_entry_matches_tables_entry():
     assert np.array_equal(oracle.gather_reduce_rows(rows, sc), oracle.gather_reduce(t, s, idx))
 
 
+# ------------------------------------------------------------ MXFP8 rows ---
+
+
+def test_e8m0_decode_matches_torch():
+    """All 256 E8M0 codes against torch's float8_e8m0fnu (a library decoder)."""
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.e8m0_value(c)
+        assert (math.isnan(v) and math.isnan(ref[c])) or v == ref[c], c
+    assert oracle.e8m0_value(127) == 1.0 and oracle.e8m0_value(0) == 2.0**-127
+
+
+def test_mx_gather_block_scales():
+    """Codes all 1.0 with block b scaled by 2^b: each module entry is
+    24 * 2^(c // 32) exactly -- catches a wrong block index or bias."""
+    T = 3
+    rows = np.full((T, 48, 256), 0x38, np.uint8)
+    esc = np.tile((127 + np.arange(8)).astype(np.uint8), (T, 48, 1))
+    mem = oracle.gather_reduce_mx_rows(rows, esc)
+    want = np.tile(24.0 * 2.0 ** (np.arange(256) // 32), 2)
+    assert np.array_equal(mem, np.tile(want, (T, 1)))
+
+
+def test_mx_gather_dense_matches_torch_decoders():
+    """MX rows as a dense product with torch's float8 decoders: exact."""
+    rng = np.random.default_rng(31)
+    T = 6
+    rows = rng.integers(0, 256, (T, 48, 256)).astype(np.uint8)
+    rows[(rows & 0x7F) == 0x7F] = 0x38
+    esc = rng.integers(120, 135, (T, 48, 8)).astype(np.uint8)
+    dec = torch.from_numpy(rows.reshape(-1)).view(torch.float8_e4m3fn).to(torch.float64).numpy().reshape(T, 48, 256)
+    sc = torch.from_numpy(esc.reshape(-1)).view(torch.float8_e8m0fnu).to(torch.float64).numpy().reshape(T, 48, 8)
+    full = dec * np.repeat(sc, 32, axis=2)
+    ref = np.concatenate([full[:, :24].sum(axis=1), full[:, 24:].sum(axis=1)], axis=1)
+    assert np.array_equal(oracle.gather_reduce_mx_rows(rows, esc), ref)
+
+
+def test_mx_row_bytes_match_page_figure():
+    """256 B of codes + 8 B of E8M0 scales = 264 B per row, 48 rows = 12,672 B."""
+    fig = _page_figures()
+    assert 48 * (256 + 8) == fig["bytes_per_token_with_scales"][0]
+    assert 256 // 32 == fig["row_scale_bytes"][0]  # one scale byte per 32-code block
+
+
 # --------------------------------------------------------------- the fuse ---
 
 
