@@ -17,6 +17,7 @@ STREAM_SCALE = 0x200  # + table j: one u32 per row, word = row
 STREAM_H = 0x300  # word = t*d + c
 STREAM_W = 0x301  # word = k*d + c
 STREAM_G = 0x302  # word = c
+STREAM_MX = 0x400  # + table j: eight u32 per row (one per E8M0 block scale), word = row*8 + b
 
 N_TABLES = 48
 ROW_BYTES = 256

@@ -101,6 +101,27 @@ __global__ void fill_scales_kernel(uint8_t *dst, uint64_t seed, int j0, int nj, 
     }
 }
 
+// E8M0 block-scale bytes of tables j0.. : byte b of row (jj, row) is
+// 125 + floor(5 u / 2^32), u = word row*8 + b of stream (seed, 0x400 + j); the
+// eight bytes go to dst + (jj*R + row)*stride + offset
+__global__ void fill_mx_scales_kernel(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, int64_t stride,
+                                      int64_t offset) {
+    const int64_t total = (int64_t)nj * R;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t jj = i / R;
+        const int64_t row = i - jj * R;
+        uint64_t out[4];
+        philox((uint64_t)row, 0, 0, 0, seed, 0x400 + (uint64_t)(j0 + jj), out);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t e = 125u + (uint32_t)(((uint64_t)word_of(out, k) * 5ull) >> 32);
+            if (k < 4) lo |= e << (8 * k); else hi |= e << (8 * (k - 4));
+        }
+        *reinterpret_cast<uint2 *>(dst + i * stride + offset) = make_uint2(lo, hi);
+    }
+}
+
 // bf16 bit patterns, words word0 .. word0+count-1 of stream (seed, stream)
 __global__ void fill_bf16_kernel(uint16_t *dst, uint64_t seed, uint64_t stream, uint64_t word0, int64_t count,
                                  const uint32_t *thr_g, const uint16_t *codes_g, int n_codes) {
@@ -151,6 +172,15 @@ extern "C" int synth_fill_scales(uint8_t *dst, uint64_t seed, int j0, int nj, in
                                  int64_t offset, void *stream) {
     fill_scales_kernel<<<grid_for((int64_t)nj * ((R + 7) / 8)), 256, 0, (cudaStream_t)stream>>>(dst, seed, j0, nj, R,
                                                                                             stride, offset);
+    return (int)cudaGetLastError();
+}
+
+extern "C" int synth_fill_mx_scales(uint8_t *dst, uint64_t seed, int j0, int nj, int64_t R, int64_t stride,
+                                    int64_t offset, void *stream) {
+    if ((stride % 8) != 0 || (offset % 8) != 0 || (reinterpret_cast<uintptr_t>(dst) % 8) != 0)
+        return (int)cudaErrorInvalidValue;
+    fill_mx_scales_kernel<<<grid_for((int64_t)nj * R), 256, 0, (cudaStream_t)stream>>>(dst, seed, j0, nj, R, stride,
+                                                                                      offset);
     return (int)cudaGetLastError();
 }
 

@@ -44,8 +44,9 @@ def _load():
         P, i64, u64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
         lib.synth_fill_tables.argtypes = [P, u64, i32, i32, i64, i64, P, P, i32, P]
         lib.synth_fill_scales.argtypes = [P, u64, i32, i32, i64, i64, i64, P]
+        lib.synth_fill_mx_scales.argtypes = [P, u64, i32, i32, i64, i64, i64, P]
         lib.synth_fill_bf16.argtypes = [P, u64, u64, u64, i64, P, P, i32, P]
-        for f in (lib.synth_fill_tables, lib.synth_fill_scales, lib.synth_fill_bf16):
+        for f in (lib.synth_fill_tables, lib.synth_fill_scales, lib.synth_fill_mx_scales, lib.synth_fill_bf16):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -99,6 +100,15 @@ def fill_record_scales(dst, seed, j0=0):
     assert rb == RECORD_BYTES and dst.dtype == torch.uint8 and dst.is_contiguous()
     _check(_load().synth_fill_scales(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, RECORD_BYTES, ROW_BYTES,
                                      _stream()))
+
+
+def fill_mx_scales(dst, seed, j0=0):
+    """The eight E8M0 block scales into bytes 256..263 of each 272-byte row of
+    dst (MXFP8-style rows: 256 e4m3 codes + one scale byte per 32 codes)."""
+    nj, R, rb = dst.shape
+    assert rb == RECORD_BYTES and dst.dtype == torch.uint8 and dst.is_contiguous()
+    _check(_load().synth_fill_mx_scales(ctypes.c_void_p(dst.data_ptr()), seed, j0, nj, R, RECORD_BYTES, ROW_BYTES,
+                                        _stream()))
 
 
 def fill_bf16(dst, seed, stream, sigma, word0=0):

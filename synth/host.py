@@ -14,6 +14,7 @@ from .configs import (
     ROW_BYTES,
     STREAM_G,
     STREAM_H,
+    STREAM_MX,
     STREAM_SCALE,
     STREAM_TABLE,
     STREAM_W,
@@ -50,6 +51,17 @@ def scales(seed, j, row):
     row = np.asarray(row, dtype=np.uint64).reshape(-1)
     u = philox_u32(np.uint64(seed), np.uint64(STREAM_SCALE) + j, row)
     return scale_from_u32(u)
+
+
+def mx_scales(seed, j, row):
+    """E8M0 block-scale bytes uint8 [n, 8] of rows (j[i], row[i]): byte b is
+    125 + floor(5 u / 2^32) for word row*8 + b of stream (seed, 0x400 + j),
+    i.e. block scales 2^-2 .. 2^2."""
+    j = np.asarray(j, dtype=np.uint64).reshape(-1)
+    row = np.asarray(row, dtype=np.uint64).reshape(-1)
+    out = philox4x64(row, 0, 0, 0, np.uint64(seed), np.uint64(STREAM_MX) + j)
+    u = out.reshape(len(row), 4).view(np.uint32).astype(np.uint64)  # little-endian: words row*8 + 0..7
+    return (125 + ((u * np.uint64(5)) >> np.uint64(32))).astype(np.uint8)
 
 
 def full_tables(seed, R):

@@ -48,6 +48,22 @@ def test_scales_range_and_exactness():
     assert big.min() >= 0.5 and big.max() < 2.0 and abs(big.mean() - 1.25) < 0.01
 
 
+def test_mx_scales_word_layout_and_range():
+    """Byte b of row r is drawn from word r*8 + b of stream 0x400 + j, mapped
+    to 125 + floor(5u / 2^32): exponents 125..129 (scales 2^-2 .. 2^2), each
+    about equally likely."""
+    j = np.array([0, 3, 47, 47])
+    r = np.array([0, 1, 999, 2**23 - 1])
+    got = host.mx_scales(7, j, r)
+    for i in range(len(j)):
+        u = philox_u32(np.uint64(7), np.uint64(0x400 + j[i]), np.uint64(r[i]) * np.uint64(8) + np.arange(8, dtype=np.uint64))
+        want = [125 + (int(x) * 5 >> 32) for x in u]
+        assert got[i].tolist() == want
+    e = host.mx_scales(1, np.zeros(40000, np.int64), np.arange(40000))
+    counts = np.bincount(e.ravel(), minlength=130)
+    assert counts[:125].sum() == 0 and np.all(np.abs(counts[125:] / e.size - 0.2) < 0.01)
+
+
 def test_rows_are_counter_addressable():
     """A row drawn alone equals the same row drawn inside a batch."""
     a = host.table_rows(3, [5, 5, 47], [0, 1000, 8388607])
