@@ -52,8 +52,12 @@ def measured_peaks():
 # Algorithmic bytes per query token of each kernel (what the method must move):
 #   gather: 4 B of token id + 48 x 256 B of rows + 48 x 4 B of scales in, 512 x 2 B of X out
 #   fuse:   512 x 2 B of X in, d x 2 B of h in, d x 2 B of h out
-def kernel_bytes_per_token(d):
-    return {"gather": 4 + 48 * 256 + 48 * 4 + 512 * 2, "fuse": 512 * 2 + 4 * d}
+def kernel_bytes_per_token(d, layout="separate"):
+    """Algorithmic bytes per query token: the gather reads one token id, 48 rows
+    of 256 code bytes plus their scales (one fp32, or eight E8M0 bytes for MX
+    rows) and writes 512 bf16; the fuse reads X and h and writes h."""
+    scale = 8 if layout == "mx" else 4
+    return {"gather": 4 + 48 * (256 + scale) + 512 * 2, "fuse": 512 * 2 + 4 * d}
 
 
 def nominal_bytes_per_token(d):
@@ -70,9 +74,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload, units):
+def ncu_traffic(kernel, workload, units, layout="separate"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    if there is none for the current kernel sources."""
+    if there is none for this workload, row layout and the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")  # JSON text
     if not os.path.exists(p):
         return None
@@ -80,6 +84,8 @@ def ncu_traffic(kernel, workload, units):
         d = json.load(f)
     e = d.get(kernel, {})
     if e.get("source_hash") != kernel_source_hash() or "bytes_per_token" not in e:
+        return None
+    if e.get("workload") != workload or e.get("layout", "separate") != layout:
         return None
     return e["bytes_per_token"] * units
 
@@ -211,9 +217,10 @@ def run_ours(args, rank, world, local_rank):
     # weak scaling: rank r draws its own token batch (tables are replicated weights)
     cfg = rank_config(base, rank)
     seeds = default_seeds()
-    record = args.layout == "record"
+    record = args.layout != "separate"  # rows carry their scales (fp32, or MX block scales)
     c = eg.make_config(cfg.V, cfg.R, cfg.d, seeds, cfg.rms_eps,
-                       row_layout=eg.ROWS_RECORD if record else eg.ROWS_SEPARATE)
+                       row_layout={"separate": eg.ROWS_SEPARATE, "record": eg.ROWS_RECORD,
+                                   "mx": eg.ROWS_MX}[args.layout])
     tok, offs = make_tokens(cfg)
     tokens = torch.from_numpy(tok).to(dev)
     seq_offsets = torch.from_numpy(offs).to(dev)
@@ -222,7 +229,9 @@ def run_ours(args, rank, world, local_rank):
     tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, **kw)
     sd.fill_tables(tables, base.seed)
     scales = None
-    if record:
+    if args.layout == "mx":
+        sd.fill_mx_scales(tables, base.seed)
+    elif record:
         sd.fill_record_scales(tables, base.seed)
     else:
         scales = torch.empty((48, cfg.R), dtype=torch.float32, **kw)
@@ -303,7 +312,7 @@ def run_ours(args, rank, world, local_rank):
             "gather": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
             "fuse": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
         }
-    kb = kernel_bytes_per_token(cfg.d)
+    kb = kernel_bytes_per_token(cfg.d, args.layout)
     kernels = {}
     for name, kms in per_kernel_ms.items():
         gbs = kb[name] * nq / (kms * 1e-3) / 1e9
@@ -312,7 +321,7 @@ def run_ours(args, rank, world, local_rank):
     if per_kernel_ms:
         dom = max(per_kernel_ms, key=per_kernel_ms.get)
         ach = kb[dom] * nq / (per_kernel_ms[dom] * 1e-3) / 1e9
-        tr = ncu_traffic(dom, args.workload, nq)
+        tr = None if (args.rows or args.tokens) else ncu_traffic(dom, args.workload, nq, args.layout)
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": tr,
                     "algorithmic_bytes_per_launch": kb[dom] * nq,
@@ -326,12 +335,15 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3->f32 gather, bf16 x bf16 -> f32 projection, bf16 residual",
-        "data": "synthetic (seeded; tables e4m3 ~ quantised N(0,1), per-row fp32 scales U[0.5,2])",
+        "data": ("synthetic (seeded; tables e4m3 ~ quantised N(0,1), "
+                 + ("E8M0 block scales 2^-2..2^2 per 32 codes)" if args.layout == "mx"
+                    else "per-row fp32 scales U[0.5,2])")),
         "config": {"workload": args.workload + (" (reduced)" if args.rows or args.tokens else ""), "V": cfg.V, "R": cfg.R, "n_seqs": cfg.n_seqs,
                    "tokens_per_step_per_gpu": cfg.t_all, "query_tokens_per_step_per_gpu": nq, "d_model": cfg.d,
                    "table_bytes": 48 * cfg.R * rb, "tables_in": "pinned host" if host else "HBM",
-                   "row_layout": ("272-byte records: 256 e4m3 codes + the row's fp32 scale" if record
-                                  else "256-byte rows + separate fp32 scale array"),
+                   "row_layout": {"record": "272-byte records: 256 e4m3 codes + the row's fp32 scale",
+                                  "mx": "272-byte MX records: 256 e4m3 codes + 8 E8M0 block scales",
+                                  "separate": "256-byte rows + separate fp32 scale array"}[args.layout],
                    "token_ids": ("uniform" if cfg.zipf_s == 0 else f"Zipf({cfg.zipf_s})"),
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world} (replicated tables)"},
         "step_roofline": {"nominal_bytes_per_token": nominal_bytes_per_token(cfg.d), "achieved_GBps": round(step_gbs, 1),
@@ -561,8 +573,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large", choices=["tiny", "decode", "prefill", "large", "host"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--layout", default="separate", choices=["record", "separate"],
-                    help="table rows that carry their scale (record) or a separate scale array")
+    ap.add_argument("--layout", default="separate", choices=["record", "separate", "mx"],
+                    help="table rows that carry their fp32 scale (record), MXFP8-style rows with eight E8M0 "
+                         "block scales (mx), or a separate scale array")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -49,6 +49,7 @@ class engram_config(ctypes.Structure):
 
 ROWS_SEPARATE = 0  # tables [48][R][256] + scales [48][R]
 ROWS_RECORD = 1  # tables [48][R][272]: 256 codes + fp32 scale at byte 256; no scales array
+ROWS_MX = 2  # tables [48][R][272]: 256 codes + 8 E8M0 block scales at bytes 256..263; no scales array
 RECORD_BYTES = 272
 
 
@@ -129,8 +130,8 @@ def _stream(stream):
 
 
 def _need(t, dtype, name, cuda=True):
-    if t is None and name in ("scales", "host_scales"):
-        return  # rows that carry their scale (ROWS_RECORD)
+    if t is None and name in ("scales", "host_scales", "staged_scales"):
+        return  # rows that carry their scales (ROWS_RECORD, ROWS_MX)
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -309,15 +310,17 @@ def engram_dedup(cfg, idx, capacity, workspace=None, unique=None, idx_staged=Non
 
 def engram_stage(cfg, host_tables, host_scales, unique, n_unique, capacity, staged_rows=None, staged_scales=None,
                  stream=None):
-    """Copy the unique rows from pinned host tables into device staging buffers."""
+    """Copy the unique rows from pinned host tables into device staging buffers
+    (256-byte rows + fp32 scales; whole 272-byte rows for ROWS_MX, scales None)."""
     _need(host_tables, torch.uint8, "host_tables", cuda=False)
     _need(host_scales, torch.float32, "host_scales", cuda=False)
     if not (host_tables.is_pinned() and (host_scales is None or host_scales.is_pinned())):
         raise ValueError("host tables and scales must be in pinned host memory")
     dev = unique.device
+    mx = cfg.row_layout == ROWS_MX  # MX rows are staged whole, with no scale array
     if staged_rows is None:
-        staged_rows = torch.empty((capacity, ROW_BYTES), dtype=torch.uint8, device=dev)
-    if staged_scales is None:
+        staged_rows = torch.empty((capacity, RECORD_BYTES if mx else ROW_BYTES), dtype=torch.uint8, device=dev)
+    if staged_scales is None and not mx:
         staged_scales = torch.empty(capacity, dtype=torch.float32, device=dev)
     _check(
         lib().engram_stage(ctypes.byref(cfg), _ptr(host_tables), _ptr(host_scales), _ptr(unique), _ptr(n_unique),

@@ -42,6 +42,12 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
     return __half22float2(*reinterpret_cast<__half2 *>(&h));
 }
 
+// OCP MX E8M0 scale byte -> 2^(e - 127) as an exact float, built from its
+// bits (e = 0 is the subnormal 2^-127, e = 255 is NaN).
+__device__ __forceinline__ float e8m0_to_float(uint32_t e) {
+    return e == 0u ? __uint_as_float(0x00400000u) : (e == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

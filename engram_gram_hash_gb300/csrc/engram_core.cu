@@ -123,10 +123,12 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
 
 enum IdxMode { IDX_I64 = 0, IDX_STAGED_I32 = 1, IDX_HASH = 2 };
 
+enum ScaleMode { SCALE_ARRAY = 0, SCALE_IN_ROW = 1, SCALE_MX = 2 };
+
 struct GatherParams {
     const uint8_t *rows;
-    const float *scales;     // separate scales, or nullptr when each row carries its scale
-    int64_t row_stride;      // 256 (codes only) or 272 (codes + fp32 scale at byte 256)
+    const float *scales;     // fp32 [rows], or nullptr when each row carries its scale bytes at byte 256
+    int64_t row_stride;      // 256 (codes only) or 272 (codes + scale bytes at byte 256)
     const void *idx;     // IDX_I64 / IDX_STAGED_I32
     int64_t n_query;
     int64_t R;           // rows per table (HBM) or staging capacity (staged)
@@ -134,9 +136,11 @@ struct GatherParams {
     HashParams hp;       // IDX_HASH
 };
 
-// 4 blocks of 256 threads per SM (at most 64 registers a thread).
-template <int kMode, bool kBf16Out>
-__global__ void __launch_bounds__(256, 4) gather_kernel(const __grid_constant__ GatherParams P) {
+// 4 blocks of 256 threads per SM (at most 64 registers a thread; 3 blocks and
+// 80 registers for kMx, which holds its scale bytes longer).  kMx: each row
+// carries eight E8M0 block scales (one per 32 codes) instead of one fp32.
+template <int kMode, bool kBf16Out, bool kMx>
+__global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_constant__ GatherParams P) {
     __shared__ uint64_t s_seed[kTables];
     if (kMode == IDX_HASH) {
         if (threadIdx.x < kTables) s_seed[threadIdx.x] = P.hp.seeds[threadIdx.x];
@@ -151,7 +155,11 @@ __global__ void __launch_bounds__(256, 4) gather_kernel(const __grid_constant__ 
     const int m = (int)(gw & 1);
     if (t >= P.n_query) return;
 
-    // lanes 0..23: this module's 24 row offsets and scales
+    // kMx: each warp's 24 rows of eight E8M0 block-scale bytes
+    __shared__ uint2 s_mx[kMx ? 8 * kTablesPerModule : 1];
+    uint2 *const wmx = s_mx + (kMx ? (threadIdx.x >> 5) * kTablesPerModule : 0);
+
+    // lanes 0..23: this module's 24 row offsets and fp32 scales
     int64_t off = 0;
     float sc = 0.f;
     int ok = 0;
@@ -173,9 +181,16 @@ __global__ void __launch_bounds__(256, 4) gather_kernel(const __grid_constant__ 
         const int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
         if (ok) {
             off = flat * P.row_stride;
-            sc = P.scales ? __ldg(P.scales + flat) : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
+            if (kMx)
+                wmx[lane] = __ldg(reinterpret_cast<const uint2 *>(P.rows + off + kRowBytes));
+            else
+                sc = P.scales ? __ldg(P.scales + flat)
+                              : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
+        } else if (kMx) {
+            wmx[lane] = make_uint2(0, 0);  // a dropped row: finite scales times zero codes
         }
     }
+    if (kMx) __syncwarp();
     const int half = lane >> 4;
     const int c16 = lane & 15;
     uint4 v[12];
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(256, 4) gather_kernel(const __grid_constant__ 
     for (int i = 0; i < 12; ++i) {
         const int src = 2 * i + half;
         const int64_t o = __shfl_sync(0xffffffffu, off, src);
-        s[i] = __shfl_sync(0xffffffffu, sc, src);
+        if (!kMx) s[i] = __shfl_sync(0xffffffffu, sc, src);
         v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 ...
         if (!__shfl_sync(0xffffffffu, ok, src)) v[i] = make_uint4(0, 0, 0, 0);  // ... and is dropped
     }
@@ -193,6 +208,8 @@ __global__ void __launch_bounds__(256, 4) gather_kernel(const __grid_constant__ 
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
 #pragma unroll
     for (int i = 0; i < 12; ++i) {
+        if (kMx)  // this lane's 16 codes sit in block c16/2 of row 2i + half
+            s[i] = e8m0_to_float(reinterpret_cast<const uint8_t *>(wmx + 2 * i + half)[c16 >> 1]);
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -361,6 +378,8 @@ __global__ void __launch_bounds__(256) dedup_remap_kernel(const int64_t *__restr
 // Each half-warp moves one 256-byte row with 16-byte loads; a warp keeps eight
 // row pairs in flight, and the grid strides over the unique list.
 
+// kWhole: rows carrying block scales are staged whole (host_stride bytes).
+template <bool kWhole>
 __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ host_tables,
                                                     const float *__restrict__ host_scales, int64_t host_stride,
                                                     const int64_t *__restrict__ unique,
@@ -382,19 +401,34 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
             v[k] = flat[k] >= 0 ? *reinterpret_cast<const uint4 *>(host_tables + flat[k] * host_stride + c16 * 16)
                                 : make_uint4(0, 0, 0, 0);
         }
-        float sc[kPairs];
+        if constexpr (kWhole) {  // each row's 16-byte tail too: lane c16 < kPairs takes that of pair c16
+            const int64_t ut = u0 + 2 * c16 + half;
+            const bool has_tail = c16 < kPairs && ut < U;
+            uint4 tail = make_uint4(0, 0, 0, 0);
+            if (has_tail)
+                tail = *reinterpret_cast<const uint4 *>(host_tables + __ldg(unique + ut) * host_stride + kRowBytes);
 #pragma unroll
-        for (int k = 0; k < kPairs; ++k)
-            sc[k] = (c16 == 0 && flat[k] >= 0)
-                        ? (host_scales ? host_scales[flat[k]]
-                                       : *reinterpret_cast<const float *>(host_tables + flat[k] * host_stride + kRowBytes))
-                        : 0.f;
+            for (int k = 0; k < kPairs; ++k) {
+                const int64_t u = u0 + 2 * k + half;
+                if (flat[k] >= 0) *reinterpret_cast<uint4 *>(staged + u * host_stride + c16 * 16) = v[k];
+            }
+            if (has_tail) *reinterpret_cast<uint4 *>(staged + ut * host_stride + kRowBytes) = tail;
+        } else {
+            float sc[kPairs];
 #pragma unroll
-        for (int k = 0; k < kPairs; ++k) {
-            const int64_t u = u0 + 2 * k + half;
-            if (flat[k] >= 0) {
-                *reinterpret_cast<uint4 *>(staged + u * kRowBytes + c16 * 16) = v[k];
-                if (c16 == 0) staged_scales[u] = sc[k];
+            for (int k = 0; k < kPairs; ++k)
+                sc[k] = (c16 == 0 && flat[k] >= 0)
+                            ? (host_scales ? host_scales[flat[k]]
+                                           : *reinterpret_cast<const float *>(host_tables + flat[k] * host_stride +
+                                                                              kRowBytes))
+                            : 0.f;
+#pragma unroll
+            for (int k = 0; k < kPairs; ++k) {
+                const int64_t u = u0 + 2 * k + half;
+                if (flat[k] >= 0) {
+                    *reinterpret_cast<uint4 *>(staged + u * kRowBytes + c16 * 16) = v[k];
+                    if (c16 == 0) staged_scales[u] = sc[k];
+                }
             }
         }
     }
@@ -420,11 +454,14 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 engram_status check_config(const engram_config *cfg) {
     if (!cfg) return ENGRAM_EINVAL;
     if (cfg->vocab < 1 || cfg->rows < 1 || cfg->d_model < 0) return ENGRAM_EINVAL;
-    if (cfg->row_layout != ENGRAM_ROWS_SEPARATE && cfg->row_layout != ENGRAM_ROWS_RECORD) return ENGRAM_EINVAL;
+    if (cfg->row_layout > ENGRAM_ROWS_MX) return ENGRAM_EINVAL;
     return ENGRAM_OK;
 }
 
-static bool records(const engram_config *cfg) { return cfg->row_layout == ENGRAM_ROWS_RECORD; }
+static bool records(const engram_config *cfg) { return cfg->row_layout != ENGRAM_ROWS_SEPARATE; }
+static bool mx(const engram_config *cfg) { return cfg->row_layout == ENGRAM_ROWS_MX; }
+// staging: MX rows are staged whole; the other layouts as 256-byte rows + fp32 scales
+static int64_t staged_stride(const engram_config *cfg) { return mx(cfg) ? ENGRAM_RECORD_BYTES : kRowBytes; }
 static int64_t row_stride(const engram_config *cfg) { return records(cfg) ? ENGRAM_RECORD_BYTES : kRowBytes; }
 // The scales argument as the kernels see it: nullptr when rows carry their scale.
 static const float *scales_arg(const engram_config *cfg, const float *scales) { return records(cfg) ? nullptr : scales; }
@@ -473,8 +510,9 @@ static void fill_hash_params(HashParams &a, const engram_config *cfg, const int3
 }
 
 // mode: IDX_I64 / IDX_STAGED_I32 / IDX_HASH; out: fp32 mem or bf16 X.
+// mx: rows carry eight E8M0 block scales at byte 256 (scales unused).
 engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const float *scales, int64_t stride,
-                            const void *idx, const HashParams *hp, int64_t n_query, int64_t R, void *out,
+                            bool mx, const void *idx, const HashParams *hp, int64_t n_query, int64_t R, void *out,
                             cudaStream_t st) {
     GatherParams P;
     memset(&P, 0, sizeof(P));
@@ -488,7 +526,13 @@ engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const 
     if (hp) P.hp = *hp;
     const int64_t warps = n_query * 2;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-#define ENGRAM_GATHER(M, B) gather_kernel<M, B><<<blocks, 256, 0, st>>>(P)
+#define ENGRAM_GATHER(M, B)                                         \
+    do {                                                             \
+        if (mx)                                                      \
+            gather_kernel<M, B, true><<<blocks, 256, 0, st>>>(P);    \
+        else                                                         \
+            gather_kernel<M, B, false><<<blocks, 256, 0, st>>>(P);   \
+    } while (0)
     if (mode == IDX_I64) {
         if (bf16_out) ENGRAM_GATHER(IDX_I64, true); else ENGRAM_GATHER(IDX_I64, false);
     } else if (mode == IDX_STAGED_I32) {
@@ -544,12 +588,18 @@ engram_status dedup_launch(const engram_config *cfg, const int64_t *idx, int64_t
     return launch_status();
 }
 
+// whole_rows: stage host_stride-byte rows as they are (MX rows); otherwise
+// 256-byte rows plus fp32 scales.
 engram_status stage_launch(const uint8_t *host_tables, const float *host_scales, int64_t host_stride,
-                           const int64_t *unique, const int64_t *n_unique, int64_t capacity, uint8_t *staged,
-                           float *staged_scales, cudaStream_t st) {
+                           bool whole_rows, const int64_t *unique, const int64_t *n_unique, int64_t capacity,
+                           uint8_t *staged, float *staged_scales, cudaStream_t st) {
     const int blocks = num_sms() * 8;
-    stage_kernel<<<blocks, 256, 0, st>>>(host_tables, host_scales, host_stride, unique, n_unique, capacity, staged,
-                                         staged_scales);
+    if (whole_rows)
+        stage_kernel<true><<<blocks, 256, 0, st>>>(host_tables, host_scales, host_stride, unique, n_unique, capacity,
+                                                   staged, staged_scales);
+    else
+        stage_kernel<false><<<blocks, 256, 0, st>>>(host_tables, host_scales, host_stride, unique, n_unique, capacity,
+                                                    staged, staged_scales);
     return launch_status();
 }
 
@@ -755,7 +805,7 @@ extern "C" engram_status engram_gather_reduce(const engram_config *cfg, const ui
     if (n_query == 0) return ENGRAM_OK;
     if (!tables || !scales_ok(cfg, scales) || !idx || !mem) return ENGRAM_EINVAL;
     if (!aligned(tables, 16) || !aligned(idx, 8) || !aligned(mem, 16)) return ENGRAM_EINVAL;
-    return gather_launch(IDX_I64, false, tables, scales_arg(cfg, scales), row_stride(cfg), idx, nullptr, n_query,
+    return gather_launch(IDX_I64, false, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), idx, nullptr, n_query,
                          cfg->rows, mem, (cudaStream_t)stream);
 }
 
@@ -779,11 +829,12 @@ extern "C" engram_status engram_stage(const engram_config *cfg, const uint8_t *h
                                       const int64_t *unique, const int64_t *n_unique, int64_t capacity,
                                       uint8_t *staged_rows, float *staged_scales, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || capacity < 1) return ENGRAM_EINVAL;
-    if (!host_tables || !scales_ok(cfg, host_scales) || !unique || !n_unique || !staged_rows || !staged_scales)
+    if (!host_tables || !scales_ok(cfg, host_scales) || !unique || !n_unique || !staged_rows ||
+        (!staged_scales && !mx(cfg)))
         return ENGRAM_EINVAL;
     if (!aligned(host_tables, 16) || !aligned(staged_rows, 16)) return ENGRAM_EINVAL;
-    return stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), unique, n_unique, capacity,
-                        staged_rows, staged_scales, (cudaStream_t)stream);
+    return stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), mx(cfg), unique, n_unique,
+                        capacity, staged_rows, staged_scales, (cudaStream_t)stream);
 }
 
 extern "C" engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_t *staged_rows,
@@ -791,10 +842,10 @@ extern "C" engram_status engram_gather_reduce_staged(const engram_config *cfg, c
                                                      int64_t n_query, int64_t capacity, float *mem, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || capacity < 1) return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
-    if (!staged_rows || !staged_scales || !idx_staged || !mem) return ENGRAM_EINVAL;
+    if (!staged_rows || (!staged_scales && !mx(cfg)) || !idx_staged || !mem) return ENGRAM_EINVAL;
     if (!aligned(staged_rows, 16) || !aligned(mem, 16) || !aligned(idx_staged, 4)) return ENGRAM_EINVAL;
-    return gather_launch(IDX_STAGED_I32, false, staged_rows, staged_scales, kRowBytes, idx_staged, nullptr, n_query,
-                         capacity, mem, (cudaStream_t)stream);
+    return gather_launch(IDX_STAGED_I32, false, staged_rows, mx(cfg) ? nullptr : staged_scales, staged_stride(cfg),
+                         mx(cfg), idx_staged, nullptr, n_query, capacity, mem, (cudaStream_t)stream);
 }
 
 extern "C" engram_status engram_fuse(const engram_config *cfg, const float *mem, const uint16_t *W_out,
@@ -829,7 +880,7 @@ extern "C" engram_status engram_forward(const engram_config *cfg, const int32_t 
     uint16_t *X = static_cast<uint16_t *>(workspace);
     HashParams hp;
     fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
-    engram_status s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), nullptr, &hp,
+    engram_status s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), nullptr, &hp,
                                     n_query, cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
@@ -847,7 +898,7 @@ extern "C" engram_status engram_gather_x(const engram_config *cfg, const int32_t
     if (n_query > (INT64_C(1) << 40)) return ENGRAM_EINVAL;
     HashParams hp;
     fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
-    return gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), nullptr, &hp, n_query,
+    return gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), nullptr, &hp, n_query,
                          cfg->rows, X, (cudaStream_t)stream);
 }
 
@@ -866,7 +917,7 @@ extern "C" size_t engram_forward_host_workspace_bytes(const engram_config *cfg, 
            + round_up((size_t)n_query * kTables * 4, 256)    // idx_staged
            + round_up((size_t)n_query * kMem * 2, 256)       // X (bf16)
            + round_up((size_t)capacity * 8, 256)             // unique
-           + round_up((size_t)capacity * kRowBytes, 256)     // staged rows
+           + round_up((size_t)capacity * staged_stride(cfg), 256)  // staged rows
            + round_up((size_t)capacity * 4, 256)             // staged scales
            + dedup_bytes(cfg);
 }
@@ -900,7 +951,7 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
     int64_t *unique = reinterpret_cast<int64_t *>(ws + o);
     o += round_up((size_t)capacity * 8, 256);
     uint8_t *rows = ws + o;
-    o += round_up((size_t)capacity * kRowBytes, 256);
+    o += round_up((size_t)capacity * staged_stride(cfg), 256);
     float *sc = reinterpret_cast<float *>(ws + o);
     o += round_up((size_t)capacity * 4, 256);
     void *dws = ws + o;
@@ -910,12 +961,13 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
     if (s != ENGRAM_OK) return s;
     if (cudaEventRecord((cudaEvent_t)ev_dedup, st) != cudaSuccess) return ENGRAM_ECUDA;
     if (cudaStreamWaitEvent(side, (cudaEvent_t)ev_dedup, 0) != cudaSuccess) return ENGRAM_ECUDA;
-    s = stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), unique, n_unique, capacity, rows, sc,
-                     side);
+    s = stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), mx(cfg), unique, n_unique, capacity,
+                     rows, sc, side);
     if (s != ENGRAM_OK) return s;
     if (cudaEventRecord((cudaEvent_t)ev_staged, side) != cudaSuccess) return ENGRAM_ECUDA;
     if (cudaStreamWaitEvent(st, (cudaEvent_t)ev_staged, 0) != cudaSuccess) return ENGRAM_ECUDA;
-    s = gather_launch(IDX_STAGED_I32, true, rows, sc, kRowBytes, idx_staged, nullptr, n_query, capacity, X, st);
+    s = gather_launch(IDX_STAGED_I32, true, rows, mx(cfg) ? nullptr : sc, staged_stride(cfg), mx(cfg), idx_staged,
+                      nullptr, n_query, capacity, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
 }
@@ -971,7 +1023,7 @@ extern "C" engram_status engram_forward_no_workspace(const engram_config *cfg, c
     // X rows [0, n_query) are all written before the projection reads them,
     // and the projection's tensor map stops at n_query rows: nothing left in
     // the array by an earlier call is read, so nothing needs clearing.
-    s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), nullptr, &hp, n_query,
+    s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), nullptr, &hp, n_query,
                       cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);

@@ -71,8 +71,16 @@ typedef enum {
  *                        contiguous read per row instead of two scattered ones
  *                        (the pages describe a row as 256 B of FP8 plus its
  *                        scales, "Engram: the table that is never multiplied"). */
+/*  ENGRAM_ROWS_MX:       MXFP8-style rows, [48][R][272]: bytes 0..255 the e4m3
+ *                        codes, 256..263 eight E8M0 block scales (byte b scales
+ *                        codes 32b..32b+31 by 2^(byte - 127); 0 is 2^-127 and
+ *                        255 is NaN), 264..271 padding; `scales` is ignored.
+ *                        This is the pages' row of 256 FP8 bytes plus 8 scale
+ *                        bytes (12,672 bytes for a token's 48 rows), in place of
+ *                        the per-row fp32 scale of the two layouts above. */
 #define ENGRAM_ROWS_SEPARATE 0
 #define ENGRAM_ROWS_RECORD 1
+#define ENGRAM_ROWS_MX 2
 #define ENGRAM_RECORD_BYTES 272
 
 typedef struct {
@@ -80,7 +88,7 @@ typedef struct {
     int32_t d_model;     /* d: residual width; engram_fuse needs d % 256 == 0 */
     int64_t rows;        /* R: rows per table, R >= 1 */
     float rms_eps;       /* eps inside the rmsnorm of the gate (1e-6 by default) */
-    uint32_t row_layout; /* ENGRAM_ROWS_SEPARATE or ENGRAM_ROWS_RECORD */
+    uint32_t row_layout; /* ENGRAM_ROWS_SEPARATE, ENGRAM_ROWS_RECORD or ENGRAM_ROWS_MX */
     uint64_t seeds[ENGRAM_N_TABLES]; /* hash seed of table j */
 } engram_config;
 
@@ -214,8 +222,10 @@ engram_status engram_dedup(const engram_config *cfg, const int64_t *idx, int64_t
  *   host_tables e4m3 [48][R][256] (or [48][R][272] records) in pinned host
  *               memory (16-byte aligned)
  *   host_scales fp32 [48][R] in pinned host memory (ENGRAM_ROWS_SEPARATE only)
- *   The staging buffers are always 256-byte rows plus a separate scale array.
- *   staged_rows [capacity][256] and staged_scales [capacity] (device)
+ *   Staging holds 256-byte rows plus a separate fp32 scale array:
+ *   staged_rows [capacity][256] and staged_scales [capacity] (device, 16-byte
+ *   aligned); for ENGRAM_ROWS_MX whole rows are staged instead:
+ *   staged_rows [capacity][272] and staged_scales unused (may be NULL).
  * Enqueued on `stream` (normally a side stream that waited for the dedup).
  */
 engram_status engram_stage(const engram_config *cfg, const uint8_t *host_tables, const float *host_scales,
@@ -226,7 +236,8 @@ engram_status engram_stage(const engram_config *cfg, const uint8_t *host_tables,
  * Step 3 over staged rows: same arithmetic, same summation order as
  * engram_gather_reduce, so its output is bit-identical to the HBM path on
  * the same inputs (SGLang's host-table mode is documented as bitwise
- * identical, "Engram: the table that is never multiplied").
+ * identical, "Engram: the table that is never multiplied").  Staging
+ * layouts as in engram_stage.
  */
 engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_t *staged_rows,
                                           const float *staged_scales, const int32_t *idx_staged,

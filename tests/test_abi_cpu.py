@@ -56,6 +56,9 @@ def test_workspace_sizes(eg):
     d = eg.engram_dedup_workspace_bytes(c)
     assert d >= 2 * 48 * cfg.R // 32 * 4
     assert eg.engram_forward_host_workspace_bytes(c, 100, 4800) >= 4800 * 256
+    # MX rows are staged whole: 272 bytes a staged row
+    cm = eg.make_config(cfg.V, cfg.R, cfg.d, default_seeds(), row_layout=eg.ROWS_MX)
+    assert eg.engram_forward_host_workspace_bytes(cm, 100, 4800) >= 4800 * 272
 
 
 def test_invalid_arguments_rejected_before_any_device_work(eg):
@@ -77,6 +80,14 @@ def test_invalid_arguments_rejected_before_any_device_work(eg):
     c3 = eg.make_config(1024, 0, 256, default_seeds())
     assert lib.engram_gather_reduce(ctypes.byref(c3), ctypes.c_void_p(256), ctypes.c_void_p(256),
                                     ctypes.c_void_p(256), 4, ctypes.c_void_p(256), null) == 1
+    # unknown row layout
+    c4 = eg.make_config(1024, 4096, 256, default_seeds(), row_layout=3)
+    assert lib.engram_gather_reduce(ctypes.byref(c4), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                                    ctypes.c_void_p(256), 4, ctypes.c_void_p(256), null) == 1
+    # MX rows: a null scales array is accepted, a null staging buffer is not
+    c5 = eg.make_config(1024, 4096, 256, default_seeds(), row_layout=eg.ROWS_MX)
+    assert lib.engram_gather_reduce_staged(ctypes.byref(c5), null, null, ctypes.c_void_p(256), 4, 16,
+                                           ctypes.c_void_p(256), null) == 1
     # zero queries is a no-op that succeeds
     assert lib.engram_hash(ctypes.byref(c), null, null, 1, 0, 0, null, null) == 0
     assert lib.engram_gather_reduce(ctypes.byref(c), null, null, null, 0, null, null) == 0

@@ -107,6 +107,33 @@ def test_host_path_record_layout(eg):
     assert torch.equal(ha.view(torch.int16), hb.view(torch.int16))
 
 
+def test_host_path_mx_layout(eg):
+    """MXFP8-style rows in pinned host memory: staged whole (byte-exact), the
+    staged gather equals the HBM gather, and the host-table forward gives the
+    HBM forward's bits and matches the oracle."""
+    a = Workload(SMALL_HOST, layout="mx")
+    b = Workload(SMALL_HOST, host_tables=True, layout="mx")
+    cap = b.cfg.tq * 48
+    idx = eg.engram_hash(b.c, b.tokens, b.seq_offsets)
+    unique, idx_staged, n_unique = eg.engram_dedup(b.c, idx, cap)
+    rows, sc = eg.engram_stage(b.c, b.tables, None, unique, n_unique, cap)
+    assert sc is None and rows.shape == (cap, 272)
+    mem_staged = eg.engram_gather_reduce_staged(b.c, rows, None, idx_staged)
+    mem_hbm = eg.engram_gather_reduce(a.c, a.tables, None, idx)
+    ha, hb = a.fresh_h(), b.fresh_h()
+    eg.engram_forward(a.c, a.tokens, a.seq_offsets, a.tables, None, a.W, a.g, ha)
+    eg.engram_forward_host(b.c, b.tokens, b.seq_offsets, b.tables, None, b.W, b.g, hb, capacity=cap)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    U = int(n_unique.item())
+    assert torch.equal(rows[:U].cpu(), b.tables.view(-1, 272)[unique[:U].cpu()])
+    assert torch.equal(mem_staged, mem_hbm)
+    assert torch.equal(ha.view(torch.int16), hb.view(torch.int16))
+    q = sample_queries(b.cfg, b.offs, 200)
+    _, _, _, ref_h, _ = b.ref_for(q)
+    check_h(hb[torch.from_numpy(q).cuda()], ref_h)
+
+
 def test_host_path_full_size(eg):
     """The host-table workload at full size (51.5 GB of pinned tables)."""
     cfg = CONFIGS["host"]

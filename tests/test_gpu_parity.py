@@ -134,6 +134,66 @@ def test_record_layout_same_bits(eg, name):
     check_h(hb, rh)
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged_prime", "prefill_small", "decode_small", "d512"])
+def test_mx_layout_small(eg, name):
+    """MXFP8-style rows (256 e4m3 codes + eight E8M0 block scales): mem and h
+    against the oracle on every query token; the split halves and the
+    separate calls give engram_forward's bits."""
+    w = Workload(SMALL[name], layout="mx")
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=w.cfg.last_n)
+    mem = eg.engram_gather_reduce(w.c, w.tables, None, idx)
+    X = eg.engram_gather_x(w.c, w.tokens, w.seq_offsets, w.tables, None, last_n=w.cfg.last_n)
+    h, h1, h2 = w.fresh_h(), w.fresh_h(), w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, None, w.W, w.g, h, last_n=w.cfg.last_n)
+    eg.engram_fuse_x(w.c, X, w.W, w.g, h1)
+    eg.engram_fuse(w.c, mem, w.W, w.g, h2)
+    _clear(eg)
+    assert torch.equal(X.view(torch.int16), mem.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(h.view(torch.int16), h1.view(torch.int16))
+    assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+    ridx, rmem, bound, rh, _ = w.ref_for(np.arange(w.cfg.tq))
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    check_mem(mem.cpu().numpy(), rmem, bound)
+    check_h(h, rh)
+
+
+def test_mx_block_scales_special_values(eg):
+    """Every code e4m3 1.0 and, per 32-column block, the E8M0 bytes 124..129,
+    0 (the subnormal 2^-127) and 255 (NaN): each mem entry is exactly
+    24 * 2^(E - 127), NaN in the last block."""
+    w = Workload(SMALL["tiny"], layout="mx")
+    w.tables[:, :, :256] = 0x38
+    e = np.array([124, 125, 126, 127, 128, 129, 0, 255], dtype=np.uint8)
+    w.tables[:, :, 256:264] = torch.from_numpy(e).cuda()
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    mem = eg.engram_gather_reduce(w.c, w.tables, None, idx)
+    _clear(eg)
+    want = np.repeat([24.0 * oracle.e8m0_value(int(x)) for x in e], 32)
+    want = np.concatenate([want, want])
+    got = mem.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got[:, :224], np.broadcast_to(want[:224], (len(got), 224)))
+    assert np.array_equal(got[:, 256:480], np.broadcast_to(want[256:480], (len(got), 224)))
+    assert np.all(np.isnan(got[:, 224:256])) and np.all(np.isnan(got[:, 480:]))
+    assert want[192] == 24.0 * 2.0 ** -127 and got[0, 192] > 0  # not flushed to zero
+    # the oracle's own MX reduction gives the same values on one token's rows
+    rows = np.full((1, 48, 256), 0x38, np.uint8)
+    ref = oracle.gather_reduce_mx_rows(rows, np.broadcast_to(e, (1, 48, 8)))
+    assert np.array_equal(ref[0, :224], want[:224])
+
+
+def test_mx_generator_twin_matches_host(eg):
+    """The device-filled E8M0 block-scale bytes equal the host draws."""
+    cfg = SMALL["ragged_prime"]
+    w = Workload(cfg, layout="mx")
+    rng = np.random.default_rng(2)
+    j = rng.integers(0, 48, 300)
+    r = rng.integers(0, cfg.R, 300)
+    got = w.tables[torch.from_numpy(j).cuda(), torch.from_numpy(r).cuda()].cpu().numpy()
+    assert np.array_equal(got[:, :256], host.table_rows(cfg.seed, j, r))
+    assert np.array_equal(got[:, 256:264], host.mx_scales(cfg.seed, j, r))
+    assert np.all(got[:, 264:] == 0)
+
+
 def test_generator_twin_rows_match_host(eg):
     """The device-filled tables/scales/h equal the host draws bit for bit."""
     cfg = SMALL["ragged_prime"]

@@ -19,7 +19,8 @@ MEM_TOL = 1e-5  # |gpu - ref| <= MEM_TOL * sum_j |term_j| on the module sums
 
 class Workload:
     """layout "separate": tables [48,R,256] + scales [48,R];
-    layout "record": tables [48,R,272] with each row's fp32 scale at byte 256 (scales None)."""
+    layout "record": tables [48,R,272] with each row's fp32 scale at byte 256 (scales None);
+    layout "mx": tables [48,R,272] with eight E8M0 block scales at bytes 256..263 (scales None)."""
 
     def __init__(self, cfg, device="cuda", tables=True, host_tables=False, layout="separate"):
         import engram_gram_hash_gb300 as eg
@@ -28,7 +29,7 @@ class Workload:
         self.dev = torch.device(device)
         self.seeds = default_seeds()
         self.layout = layout
-        rl = eg.ROWS_RECORD if layout == "record" else eg.ROWS_SEPARATE
+        rl = {"separate": eg.ROWS_SEPARATE, "record": eg.ROWS_RECORD, "mx": eg.ROWS_MX}[layout]
         self.c = eg.make_config(cfg.V, cfg.R, cfg.d, self.seeds, cfg.rms_eps, row_layout=rl)
         self.tok, self.offs = make_tokens(cfg)
         self.qpos = query_positions(cfg, self.offs)
@@ -36,7 +37,7 @@ class Workload:
         self.seq_offsets = torch.from_numpy(self.offs).to(self.dev)
         self.tables = self.scales = None
         if tables:
-            rb = 272 if layout == "record" else 256
+            rb = 256 if layout == "separate" else 272
             if host_tables:
                 self.tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, pin_memory=True)
             else:
@@ -44,6 +45,8 @@ class Workload:
             sd.fill_tables(self.tables, cfg.seed)
             if layout == "record":
                 sd.fill_record_scales(self.tables, cfg.seed)
+            elif layout == "mx":
+                sd.fill_mx_scales(self.tables, cfg.seed)
             else:
                 kw = {"pin_memory": True} if host_tables else {"device": self.dev}
                 self.scales = torch.empty((48, cfg.R), dtype=torch.float32, **kw)
@@ -70,9 +73,14 @@ class Workload:
         idx = oracle.hash_positions(self.tok, self.offs, cfg.V, cfg.R, self.seeds, self.qpos[q_sel])
         jj = np.tile(np.arange(48), len(q_sel))
         rows = host.table_rows(cfg.seed, jj, idx.reshape(-1)).reshape(len(q_sel), 48, 256)
-        sc = host.scales(cfg.seed, jj, idx.reshape(-1)).reshape(len(q_sel), 48)
-        mem = oracle.gather_reduce_rows(rows, sc)
-        bound = oracle.gather_reduce_rows(rows & 0x7F, sc)  # sum_j |term_j|
+        if self.layout == "mx":
+            esc = host.mx_scales(cfg.seed, jj, idx.reshape(-1)).reshape(len(q_sel), 48, 8)
+            mem = oracle.gather_reduce_mx_rows(rows, esc)
+            bound = oracle.gather_reduce_mx_rows(rows & 0x7F, esc)  # sum_j |term_j|
+        else:
+            sc = host.scales(cfg.seed, jj, idx.reshape(-1)).reshape(len(q_sel), 48)
+            mem = oracle.gather_reduce_rows(rows, sc)
+            bound = oracle.gather_reduce_rows(rows & 0x7F, sc)  # sum_j |term_j|
         h0 = host.h_rows(cfg.seed, cfg.d, q_sel)
         hn, gate = oracle.fuse(mem, host.w_out(cfg.seed, cfg.d), host.g_vec(cfg.seed, cfg.d), h0, cfg.rms_eps)
         return idx, mem, bound, hn, gate
