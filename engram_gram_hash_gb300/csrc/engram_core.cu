@@ -137,7 +137,7 @@ struct GatherParams {
 };
 
 // 4 blocks of 256 threads per SM (at most 64 registers a thread; 3 blocks and
-// 80 registers for kMx, which holds its scale bytes longer).  kMx: each row
+// 80 registers for kMx, which also holds twelve scale bytes a lane).  kMx: each row
 // carries eight E8M0 block scales (one per 32 codes) instead of one fp32.
 template <int kMode, bool kBf16Out, bool kMx>
 __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_constant__ GatherParams P) {
@@ -154,10 +154,6 @@ __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_c
     const int64_t t = gw >> 1;
     const int m = (int)(gw & 1);
     if (t >= P.n_query) return;
-
-    // kMx: each warp's 24 rows of eight E8M0 block-scale bytes
-    __shared__ uint2 s_mx[kMx ? 8 * kTablesPerModule : 1];
-    uint2 *const wmx = s_mx + (kMx ? (threadIdx.x >> 5) * kTablesPerModule : 0);
 
     // lanes 0..23: this module's 24 row offsets and fp32 scales
     int64_t off = 0;
@@ -181,35 +177,34 @@ __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_c
         const int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
         if (ok) {
             off = flat * P.row_stride;
-            if (kMx)
-                wmx[lane] = __ldg(reinterpret_cast<const uint2 *>(P.rows + off + kRowBytes));
-            else
+            if (!kMx)
                 sc = P.scales ? __ldg(P.scales + flat)
                               : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
-        } else if (kMx) {
-            wmx[lane] = make_uint2(0, 0);  // a dropped row: finite scales times zero codes
         }
     }
-    if (kMx) __syncwarp();
     const int half = lane >> 4;
     const int c16 = lane & 15;
     uint4 v[12];
     float s[12];
+    uint32_t sb[12];  // kMx: the E8M0 byte of the block holding this lane's 16 codes (block c16/2)
 #pragma unroll
     for (int i = 0; i < 12; ++i) {
         const int src = 2 * i + half;
         const int64_t o = __shfl_sync(0xffffffffu, off, src);
         if (!kMx) s[i] = __shfl_sync(0xffffffffu, sc, src);
+        if (kMx) sb[i] = __ldg(P.rows + o + kRowBytes + (c16 >> 1));
         v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 ...
-        if (!__shfl_sync(0xffffffffu, ok, src)) v[i] = make_uint4(0, 0, 0, 0);  // ... and is dropped
+        if (!__shfl_sync(0xffffffffu, ok, src)) {   // ... and is dropped (a finite scale times zero codes)
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (kMx) sb[i] = 0;
+        }
     }
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
 #pragma unroll
     for (int i = 0; i < 12; ++i) {
-        if (kMx)  // this lane's 16 codes sit in block c16/2 of row 2i + half
-            s[i] = e8m0_to_float(reinterpret_cast<const uint8_t *>(wmx + 2 * i + half)[c16 >> 1]);
+        if (kMx) s[i] = e8m0_to_float(sb[i]);
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -736,7 +731,7 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     if (p.cpg > 16) return ENGRAM_EINVAL;
     CUtensorMap wmap, xmap;
     memset(&xmap, 0, sizeof(xmap));
-    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, fuse::BK)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
+    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, fuse::WBK)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
     if (x_bf16) {
         if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
             return cuda_fail(cudaErrorInvalidValue, "X tensor map");

@@ -31,13 +31,16 @@ namespace fuse {
 
 constexpr int BM = 128;                            // tokens per tile (TMEM lanes)
 constexpr int BN = 256;                            // d columns per chunk (MMA N)
-constexpr int BK = 64;                             // K rows per W stage
-constexpr int KSTAGES = kMem / BK;                 // 8 W stages per chunk
-constexpr int NSTAGE = 2;                          // W ring depth
+constexpr int BK = 64;                             // K columns per X block (one 128-byte swizzle row)
+constexpr int KSTAGES = kMem / BK;                 // 8 X blocks
+constexpr int WBK = 64;                            // K rows per W stage
+constexpr int WSTAGES = kMem / WBK;                // W stages per chunk
+constexpr int W_RING_BYTES = 64 * 1024;            // W ring
 constexpr int X_KBLOCK_BYTES = BM * BK * 2;        // 16 KB: 128 rows x 128 B
 constexpr int X_BYTES = X_KBLOCK_BYTES * KSTAGES;  // 128 KB
-constexpr int W_BOX_BYTES = BK * 64 * 2;           // 8 KB: 64 K-rows x 64 N
-constexpr int W_STAGE_BYTES = W_BOX_BYTES * (BN / 64);  // 32 KB
+constexpr int W_BOX_BYTES = WBK * 64 * 2;          // WBK K-rows x 64 N
+constexpr int W_STAGE_BYTES = W_BOX_BYTES * (BN / 64);
+constexpr int NSTAGE = W_RING_BYTES / W_STAGE_BYTES;  // W ring depth
 constexpr int TMEM_COLS = 2 * BN;                  // two accumulators
 constexpr int EPI_WARPS = 8;                       // two per TMEM lane quadrant
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;   // warp0 TMA, warp1 MMA, warps 2..9 epilogue
@@ -66,6 +69,7 @@ struct Shared {
 // 1024-byte aligned (swizzle atoms).
 constexpr int SMEM_BYTES = X_BYTES + NSTAGE * W_STAGE_BYTES + EPI_WARPS * STAGE_BYTES + (int)sizeof(Shared);
 static_assert(SMEM_BYTES <= 232448, "fuse kernel shared memory over the per-CTA limit");
+static_assert(WBK % 16 == 0 && BK % WBK == 0 && W_RING_BYTES % W_STAGE_BYTES == 0 && NSTAGE >= 2, "W ring shape");
 
 struct Params {
     const float *mem;  // [n_query][512] fp32 (X_FROM_F32_MEM)
@@ -148,13 +152,13 @@ __global__ void __maxnreg__(168)  // 10 warps: 3 share a sub-partition (16K regi
                     x_issued = true;
                 }
                 for (int c = c0; c < c0 + CPG && !*abort; ++c) {
-                    for (int ks = 0; ks < KSTAGES; ++ks) {
+                    for (int ks = 0; ks < WSTAGES; ++ks) {
                         if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort)) break;
                         mbar_arrive_expect_tx(&sh->full[stage], W_STAGE_BYTES);
                         uint8_t *dst = w_smem + stage * W_STAGE_BYTES;
 #pragma unroll
                         for (int b = 0; b < BN / 64; ++b)
-                            tma_load_2d(dst + b * W_BOX_BYTES, &w_map, &sh->full[stage], c * BN + b * 64, ks * BK);
+                            tma_load_2d(dst + b * W_BOX_BYTES, &w_map, &sh->full[stage], c * BN + b * 64, ks * WBK);
                         issued[stage] = true;
                         issued_parity[stage] = phase;
                         if (++stage == NSTAGE) {
@@ -190,14 +194,15 @@ __global__ void __maxnreg__(168)  // 10 warps: 3 share a sub-partition (16K regi
                     if (!mbar_wait(&sh->acc_empty[buf], (use & 1u) ^ 1u, abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int ks = 0; ks < KSTAGES; ++ks) {
+                    for (int ks = 0; ks < WSTAGES; ++ks) {
                         if (!mbar_wait(&sh->full[stage], phase, abort)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
-                        for (int s = 0; s < BK / 16; ++s) {
-                            // A: K-block ks, K-step s = 32 bytes into each 128-byte swizzled row
-                            const uint64_t adesc =
-                                smem_desc(x_addr + ks * X_KBLOCK_BYTES + s * 32, 16, 1024, kSwizzle128B);
+                        for (int s = 0; s < WBK / 16; ++s) {
+                            // A: K-step kk = 16 columns; X block kk/4, 32 bytes per step into each 128-byte row
+                            const int kk = ks * (WBK / 16) + s;
+                            const uint64_t adesc = smem_desc(x_addr + (kk >> 2) * X_KBLOCK_BYTES + (kk & 3) * 32, 16,
+                                                             1024, kSwizzle128B);
                             // B: 16 K-rows (2 x 8-row groups of 1 KB) further; N atoms of 64 are 8 KB apart
                             const uint64_t bdesc =
                                 smem_desc(w_addr + stage * W_STAGE_BYTES + s * 2048, W_BOX_BYTES, 1024, kSwizzle128B);
