@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "fuse.cuh"
+#include "fuse2.cuh"
 
 namespace engram {
 
@@ -655,15 +656,32 @@ static int pick_groups(int64_t m_tiles, int n_chunks) {
     return best;
 }
 
-template <int XSRC, int CPG>
+// Projection kernels: X from fp32 mem (fuse.cuh), X by TMA with the gate on
+// the update warps (fuse.cuh), X by TMA with the gate on its own warps (fuse2.cuh).
+enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X = 1, FUSE_BF16_X_GATE_WARPS = 2 };
+constexpr FuseKind kBf16XKernel = FUSE_BF16_X_GATE_WARPS;
+
+template <int KIND, int CPG>
+static auto fuse_kernel_for() {
+    if constexpr (KIND == FUSE_F32_MEM)
+        return fuse::fuse_kernel<fuse::X_FROM_F32_MEM, CPG>;
+    else if constexpr (KIND == FUSE_BF16_X)
+        return fuse::fuse_kernel<fuse::X_FROM_BF16_TMA, CPG>;
+    else
+        return fuse2::fuse2_kernel<CPG>;
+}
+
+template <int KIND, int CPG>
 static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
                                    cudaStream_t st) {
-    auto kern = fuse::fuse_kernel<XSRC, CPG>;
+    auto kern = fuse_kernel_for<KIND, CPG>();
+    constexpr int kThreads = KIND == FUSE_BF16_X_GATE_WARPS ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
+    constexpr int kSmem = KIND == FUSE_BF16_X_GATE_WARPS ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fuse::SMEM_BYTES);
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fuse smem)");
         attr_done[dev] = true;
     }
@@ -673,8 +691,8 @@ static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &x
     attr[0].val.clusterDim.x = p.groups;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(fuse::NUM_THREADS);
-    cfg.dynamicSmemBytes = fuse::SMEM_BYTES;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -697,15 +715,15 @@ static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &x
     return launch_status();
 }
 
-template <int XSRC>
+template <int KIND>
 static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
                                    cudaStream_t st) {
     switch (p.cpg) {
-        case 1: return fuse_launch_t<XSRC, 1>(wmap, xmap, p, st);
-        case 2: return fuse_launch_t<XSRC, 2>(wmap, xmap, p, st);
-        case 4: return fuse_launch_t<XSRC, 4>(wmap, xmap, p, st);
-        case 8: return fuse_launch_t<XSRC, 8>(wmap, xmap, p, st);
-        case 16: return fuse_launch_t<XSRC, 16>(wmap, xmap, p, st);
+        case 1: return fuse_launch_t<KIND, 1>(wmap, xmap, p, st);
+        case 2: return fuse_launch_t<KIND, 2>(wmap, xmap, p, st);
+        case 4: return fuse_launch_t<KIND, 4>(wmap, xmap, p, st);
+        case 8: return fuse_launch_t<KIND, 8>(wmap, xmap, p, st);
+        case 16: return fuse_launch_t<KIND, 16>(wmap, xmap, p, st);
     }
     return ENGRAM_EINVAL;
 }
@@ -731,13 +749,15 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     if (p.cpg > 16) return ENGRAM_EINVAL;
     CUtensorMap wmap, xmap;
     memset(&xmap, 0, sizeof(xmap));
-    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, fuse::WBK)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
+    // W boxes: 64 columns x WBK K-rows (fuse.cuh) or x BK K-rows (fuse2.cuh, one ring stage)
+    const uint32_t w_box_rows = (x_bf16 && kBf16XKernel == FUSE_BF16_X_GATE_WARPS) ? fuse::BK : fuse::WBK;
+    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, w_box_rows)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
     if (x_bf16) {
         if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
             return cuda_fail(cudaErrorInvalidValue, "X tensor map");
-        return fuse_dispatch<fuse::X_FROM_BF16_TMA>(wmap, xmap, p, st);
+        return fuse_dispatch<kBf16XKernel>(wmap, xmap, p, st);
     }
-    return fuse_dispatch<fuse::X_FROM_F32_MEM>(wmap, xmap, p, st);
+    return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, p, st);
 }
 
 engram_status check_fuse_args(const engram_config *cfg, const void *W, const void *g, const void *h) {
