@@ -19,6 +19,7 @@
 #include "common.cuh"
 #include "fuse.cuh"
 #include "fuse2.cuh"
+#include "fuse3.cuh"
 
 namespace engram {
 
@@ -656,17 +657,60 @@ static int pick_groups(int64_t m_tiles, int n_chunks) {
     return best;
 }
 
-// Projection kernels: X from fp32 mem (fuse.cuh), X by TMA with the gate on
-// the update warps (fuse.cuh), X by TMA with the gate on its own warps (fuse2.cuh).
-enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X = 1, FUSE_BF16_X_GATE_WARPS = 2 };
-constexpr FuseKind kBf16XKernel = FUSE_BF16_X_GATE_WARPS;
+// Projection kernels: X converted from fp32 mem in the kernel (fuse.cuh);
+// X by TMA with the gate on its own warps (fuse2.cuh, many tiles); X by TMA
+// with the h slice held in shared memory (fuse3.cuh, few tiles: d slices of 1
+// or 2 chunks).  For the same split of d all three give the same bits.
+enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X_GATE_WARPS = 2 };
+
+// Persistent cluster launch: as many clusters of `groups` CTAs as fit at once
+// (cached per device and cluster size in *max_clusters), each striding over
+// the tiles.  attr_done / max_clusters belong to one kernel instantiation.
+template <typename Kern, typename... Args>
+static engram_status launch_persistent(Kern kern, int threads, int smem, int groups, int64_t m_tiles,
+                                       bool *attr_done, int (*max_clusters)[fuse::MAX_GROUPS + 1], cudaStream_t st,
+                                       const Args &...args) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool cache = dev >= 0 && dev < 64;
+    if (!cache || !attr_done[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fuse smem)");
+        if (cache) attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = groups;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int mc = cache ? max_clusters[dev][groups] : 0;
+    if (mc == 0) {
+        cfg.gridDim = dim3(groups * 64);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms() / groups;
+        }
+        mc = n;
+        if (cache) max_clusters[dev][groups] = n;
+    }
+    const int64_t clusters = std::min<int64_t>(m_tiles, mc);
+    cfg.gridDim = dim3((unsigned)(clusters * groups));
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(fuse)");
+    return launch_status();
+}
 
 template <int KIND, int CPG>
 static auto fuse_kernel_for() {
     if constexpr (KIND == FUSE_F32_MEM)
         return fuse::fuse_kernel<fuse::X_FROM_F32_MEM, CPG>;
-    else if constexpr (KIND == FUSE_BF16_X)
-        return fuse::fuse_kernel<fuse::X_FROM_BF16_TMA, CPG>;
     else
         return fuse2::fuse2_kernel<CPG>;
 }
@@ -674,45 +718,12 @@ static auto fuse_kernel_for() {
 template <int KIND, int CPG>
 static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
                                    cudaStream_t st) {
-    auto kern = fuse_kernel_for<KIND, CPG>();
     constexpr int kThreads = KIND == FUSE_BF16_X_GATE_WARPS ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
     constexpr int kSmem = KIND == FUSE_BF16_X_GATE_WARPS ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
     static bool attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fuse smem)");
-        attr_done[dev] = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.groups;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // persistent: as many clusters as fit at once, each striding over tiles
     static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
-    int &mc = max_clusters[dev][p.groups];
-    if (mc == 0) {
-        cfg.gridDim = dim3(p.groups * 64);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-            cudaGetLastError();
-            n = num_sms() / p.groups;
-        }
-        mc = n;
-    }
-    const int64_t clusters = std::min<int64_t>(p.m_tiles, mc);
-    cfg.gridDim = dim3((unsigned)(clusters * p.groups));
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, wmap, xmap, p);
-    if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(fuse)");
-    return launch_status();
+    return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
+                             max_clusters, st, wmap, xmap, p);
 }
 
 template <int KIND>
@@ -728,6 +739,25 @@ static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &x
     return ENGRAM_EINVAL;
 }
 
+template <int CPG>
+static engram_status fuse3_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hl,
+                                    const CUtensorMap &hs, const fuse::Params &p, cudaStream_t st) {
+    static bool attr_done[64] = {};
+    static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
+    return launch_persistent(fuse3::fuse3_kernel<CPG>, fuse3::NUM_THREADS, fuse3::smem_bytes<CPG>(), p.groups,
+                             p.m_tiles, attr_done, max_clusters, st, wmap, xmap, hl, hs, p);
+}
+
+// Few tiles (under one per two SMs): the h-resident kernel, with d split into
+// slices of 1 chunk if that fits a cluster of 8, else 2.  Returns its chunks
+// per CTA, or 0 to use the other kernels (many tiles, or d too wide).
+static int pick_cpg_h_resident(int64_t m_tiles, int n_chunks) {
+    if (m_tiles * 2 >= num_sms()) return 0;
+    if (n_chunks <= fuse::MAX_GROUPS) return 1;
+    if (n_chunks % 2 == 0 && n_chunks / 2 <= fuse::MAX_GROUPS) return 2;
+    return 0;
+}
+
 // y = X @ W_out and the gated residual update.  X comes either from fp32 mem
 // (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
 engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint16_t *x_bf16, const uint16_t *W,
@@ -741,7 +771,9 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     p.n_query = n_query;
     p.m_tiles = (n_query + fuse::BM - 1) / fuse::BM;
     p.d = d;
-    p.groups = pick_groups(p.m_tiles, n_chunks);
+    // One split of d for both inputs (fp32 mem or bf16 X), so they agree bit for bit.
+    const int cpg3 = pick_cpg_h_resident(p.m_tiles, n_chunks);
+    p.groups = cpg3 ? n_chunks / cpg3 : pick_groups(p.m_tiles, n_chunks);
     if (p.groups == 0) return ENGRAM_EINVAL;
     p.cpg = n_chunks / p.groups;
     p.eps = cfg->rms_eps;
@@ -750,12 +782,19 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     CUtensorMap wmap, xmap;
     memset(&xmap, 0, sizeof(xmap));
     // W boxes: 64 columns x WBK K-rows (fuse.cuh) or x BK K-rows (fuse2.cuh, one ring stage)
-    const uint32_t w_box_rows = (x_bf16 && kBf16XKernel == FUSE_BF16_X_GATE_WARPS) ? fuse::BK : fuse::WBK;
+    const uint32_t w_box_rows = x_bf16 ? fuse::BK : fuse::WBK;
     if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, w_box_rows)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
     if (x_bf16) {
         if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
             return cuda_fail(cudaErrorInvalidValue, "X tensor map");
-        return fuse_dispatch<kBf16XKernel>(wmap, xmap, p, st);
+        if (cpg3 != 0) {
+            CUtensorMap hl, hs;  // h slice boxes: 64 columns x 128 tokens (loads) / x 32 tokens (stores)
+            if (!bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, 64, fuse::BM) ||
+                !bf16_map_2d(&hs, h, (uint64_t)d, (uint64_t)n_query, 64, 32))
+                return cuda_fail(cudaErrorInvalidValue, "h tensor map");
+            return cpg3 == 1 ? fuse3_launch_t<1>(wmap, xmap, hl, hs, p, st) : fuse3_launch_t<2>(wmap, xmap, hl, hs, p, st);
+        }
+        return fuse_dispatch<FUSE_BF16_X_GATE_WARPS>(wmap, xmap, p, st);
     }
     return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, p, st);
 }

@@ -1,4 +1,8 @@
 // The gated projection into the residual stream on tcgen05 tensor cores.
+// This kernel serves the fp32 mem input (engram_fuse), converting it to the
+// bf16 X tile in shared memory; a bf16 X from the gather goes to fuse2.cuh
+// (many tiles) or fuse3.cuh (few tiles), which share its tile, split and
+// arithmetic.
 //
 // Work split: a tile is 128 query tokens; a thread-block cluster of G CTAs
 // shares a tile and splits d into G slices of d/G columns.  Every CTA holds

@@ -194,6 +194,28 @@ def test_mx_generator_twin_matches_host(eg):
     assert np.all(got[:, 264:] == 0)
 
 
+def test_many_tiles_forward(eg):
+    """83 tiles of 128 tokens at d = 4096 (the many-tile projection kernel):
+    engram_forward and engram_gather_x + engram_fuse_x give the bits of
+    hash + gather + fuse from fp32 mem, and h matches the oracle on a seeded
+    sample plus every sequence start and the last token."""
+    cfg = CONFIGS["prefill"].with_(seq_lens=(6000, 4500), R=1 << 16, seed=8)
+    w = Workload(cfg)
+    h1, h2, h3 = w.fresh_h(), w.fresh_h(), w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h1)
+    X = eg.engram_gather_x(w.c, w.tokens, w.seq_offsets, w.tables, w.scales)
+    eg.engram_fuse_x(w.c, X, w.W, w.g, h2)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    eg.engram_fuse(w.c, mem, w.W, w.g, h3)
+    _clear(eg)
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    assert torch.equal(h1.view(torch.int16), h3.view(torch.int16))
+    q = sample_queries(cfg, w.offs, 256)
+    _, _, _, rh, _ = w.ref_for(q)
+    check_h(h1[torch.from_numpy(q).cuda()], rh)
+
+
 def test_generator_twin_rows_match_host(eg):
     """The device-filled tables/scales/h equal the host draws bit for bit."""
     cfg = SMALL["ragged_prime"]
