@@ -53,6 +53,10 @@ constexpr int RING_STAGE_BYTES = X_KBLOCK_BYTES + W_BOX_BYTES * (BN / 64);  // 1
 constexpr int NSTAGE = 4;
 
 constexpr int UPDATE_WARPS = 8;  // warps 4..11
+// The gate warps start reading tile i+1 once the update warps have finished
+// chunk LEAD_CHUNK of tile i (-1: as soon as they start tile i).  A shorter
+// lead keeps the gate warps' h reads in L2 until the update warps re-read them.
+constexpr int LEAD_CHUNK = 0;
 constexpr int GATE_WARPS = 6;    // warps 2, 3, 12..15
 constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
@@ -64,6 +68,7 @@ struct Shared {
     uint64_t acc_empty[2];
     uint64_t part_full[2];
     uint64_t part_free[2];
+    uint64_t upd_mark[2];  // local: the update warps reached chunk LEAD_CHUNK of a tile
     uint64_t done;
     uint32_t tmem_base;
     int abort;
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&sh->acc_empty[b], UPDATE_WARPS);
             mbar_init(&sh->part_full[b], GATE_WARPS * p.groups);
             mbar_init(&sh->part_free[b], UPDATE_WARPS * p.groups);
+            mbar_init(&sh->upd_mark[b], UPDATE_WARPS);
         }
         mbar_init(&sh->done, 1);
         sh->abort = 0;
@@ -224,6 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) {  // this warp is done with part[pb] of every CTA
                 const uint32_t bar = smem_u32(&sh->part_free[pb]);
                 for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+                if (LEAD_CHUNK < 0 || LEAD_CHUNK >= CPG) mbar_arrive(&sh->upd_mark[pb]);
             }
 
             // h = bf16(h + gate * y) on this warp's 32 rows and 128 columns of
@@ -295,7 +302,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (sub == 1) {
                     tc_fence_before();
-                    if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
+                    if (lane == 0) {
+                        mbar_arrive(&sh->acc_empty[buf]);
+                        if (c == LEAD_CHUNK) mbar_arrive(&sh->upd_mark[pb]);
+                    }
                 }
             }
             acc_it += CPG;
@@ -315,6 +325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t pb = it & 1u;
             const uint32_t use = it >> 1;
             if (use > 0 && !mbar_wait_cluster(&sh->part_free[pb], (use - 1u) & 1u, abort)) break;
+            if (it > 0 && !mbar_wait(&sh->upd_mark[pb ^ 1u], ((it - 1u) >> 1) & 1u, abort)) break;
             for (int b = gw; b < NB; b += GATE_WARPS) {
                 const int rbase = b * RB;
                 uint4 hv[RB][CPG];
