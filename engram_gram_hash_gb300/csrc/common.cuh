@@ -159,6 +159,21 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// L2 cache policy that keeps lines longer than normal ones (for data read
+// again soon by another warp), and a 16-byte load that applies it.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ld_v4_l2_hint(const void *p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 // Tiled TMA store of one box from shared memory (bulk async-group of the
 // issuing thread); rows or columns outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int x, int y) {

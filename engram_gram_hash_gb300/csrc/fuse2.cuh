@@ -315,8 +315,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // --------------------------------------------------- gate warps -----
         // Rows in batches of RB (16 16-byte loads per lane in flight), batch b
         // on gate warp b mod 6.  Lanes stride over each row's 16-byte pieces;
-        // g is re-read per batch (L1) rather than held in registers.
+        // g is re-read per batch (L1) rather than held in registers.  The h
+        // lines are loaded with an L2 evict-last hint: the update warps read
+        // them again within the next tile.
         const int gw = gate_warp_index(warp);
+        const uint64_t keep = l2_policy_evict_last();  // the update warps re-read these lines
         constexpr int RB = 16 / CPG;
         constexpr int NB = BM / RB;
         uint32_t it = 0;
@@ -334,9 +337,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int64_t t = m0 + rbase + r;
 #pragma unroll
                     for (int k = 0; k < CPG; ++k)
-                        hv[r][k] = t < p.n_query
-                                       ? *reinterpret_cast<const uint4 *>(p.h + t * p.d + col0 + (lane + 32 * k) * 8)
-                                       : make_uint4(0, 0, 0, 0);
+                        hv[r][k] = t < p.n_query ? ld_v4_l2_hint(p.h + t * p.d + col0 + (lane + 32 * k) * 8, keep)
+                                                 : make_uint4(0, 0, 0, 0);
                 }
                 float s[RB], d[RB];
 #pragma unroll
