@@ -216,6 +216,32 @@ def test_many_tiles_forward(eg):
     check_h(h1[torch.from_numpy(q).cuda()], rh)
 
 
+@pytest.mark.parametrize("name", ["decode_small", "tiny"])
+def test_forward_in_cuda_graph(eg, name):
+    """engram_forward captured once in a CUDA graph and replayed gives the bits
+    of the same call launched eagerly (no host sync or allocation inside)."""
+    w = Workload(SMALL[name])
+    nq = w.cfg.tq
+    ws = torch.empty(max(eg.engram_forward_workspace_bytes(w.c, nq), 1), dtype=torch.uint8, device="cuda")
+    h1, h2 = w.fresh_h(), w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h1, last_n=w.cfg.last_n,
+                      n_query=nq, workspace=ws)
+    h_warm = w.fresh_h()  # first-call set-up (function attributes, occupancy) before capture
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h_warm, last_n=w.cfg.last_n,
+                      n_query=nq, workspace=ws)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h2, last_n=w.cfg.last_n,
+                          n_query=nq, workspace=ws)
+    graph.replay()
+    _clear(eg)
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    graph.replay()  # a second replay applies the update again
+    torch.cuda.synchronize()
+    assert not torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+
+
 def test_generator_twin_rows_match_host(eg):
     """The device-filled tables/scales/h equal the host draws bit for bit."""
     cfg = SMALL["ragged_prime"]
