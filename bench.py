@@ -237,6 +237,38 @@ def time_forward_graph(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g
             "graph_us_per_step": round(graph_us, 2), "steps": reps}
 
 
+def time_host_pipelined(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev, chunk, steps):
+    """The chunked, pipelined host-table forward: ms per step and rows staged."""
+    import torch
+
+    cap = chunk * 48
+    ws = torch.empty(eg.engram_forward_host_pipelined_workspace_bytes(c, nq, chunk, cap), dtype=torch.uint8,
+                     device=dev)
+    n_unique = torch.zeros(-(-nq // chunk), dtype=torch.int64, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    events = [torch.cuda.Event() for _ in range(6)]
+
+    def fwd():
+        eg.engram_forward_host_pipelined(c, tokens, seq_offsets, tables, scales, W, g, h, chunk, capacity=cap,
+                                         last_n=cfg.last_n, n_query=nq, workspace=ws, n_unique=n_unique,
+                                         side_stream=side, events=events)
+
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fwd()
+    b.record()
+    torch.cuda.synchronize()
+    if eg.engram_last_error() != 0:
+        raise RuntimeError("device error in the pipelined host path")
+    ms = a.elapsed_time(b) / steps
+    return {"chunk": chunk, "ms_per_step": round(ms, 4), "tokens_per_s": round(nq / (ms * 1e-3), 1),
+            "rows_staged_per_step": int(n_unique.sum().item()), "steps": steps}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -265,7 +297,11 @@ def run_ours(args, rank, world, local_rank):
     seq_offsets = torch.from_numpy(offs).to(dev)
     rb = eg.RECORD_BYTES if record else 256
     kw = {"pin_memory": True} if cfg.host_tables else {"device": dev}
-    tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, **kw)
+    huge = cfg.host_tables and args.host_alloc == "huge"
+    if huge:  # pinned, on transparent huge pages (engram_host_alloc), zeroed
+        tables = eg.host_tables_empty((48, cfg.R, rb), torch.uint8)
+    else:
+        tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, **kw)
     sd.fill_tables(tables, base.seed)
     scales = None
     if args.layout == "mx":
@@ -273,7 +309,8 @@ def run_ours(args, rank, world, local_rank):
     elif record:
         sd.fill_record_scales(tables, base.seed)
     else:
-        scales = torch.empty((48, cfg.R), dtype=torch.float32, **kw)
+        scales = (eg.host_tables_empty((48, cfg.R), torch.float32) if huge
+                  else torch.empty((48, cfg.R), dtype=torch.float32, **kw))
         sd.fill_scales(scales, base.seed)
     W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=dev)
     g = torch.empty(cfg.d, dtype=torch.bfloat16, device=dev)
@@ -404,6 +441,11 @@ def run_ours(args, rank, world, local_rank):
         out["cuda_graph"] = cuda_graph
     if host:
         out["config"]["n_unique_rows"] = int(n_unique.item())
+        out["config"]["host_memory"] = ("pinned, transparent huge pages (engram_host_alloc)" if huge
+                                        else "pinned (cudaHostAlloc via torch)")
+        out["pipelined"] = [time_host_pipelined(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
+                                                ch, max(3, min(K, 20)))
+                            for ch in args.host_chunks if 0 < ch < nq]
     if not args.no_e2e:
         out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -632,6 +674,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--host-alloc", default="huge", choices=["huge", "torch"],
+                    help="host tables in engram_host_alloc memory (huge pages) or torch pinned memory")
+    ap.add_argument("--host-chunks", type=int, nargs="*", default=[32768],
+                    help="chunk sizes for the pipelined host-table path (host workload)")
     ap.add_argument("--probe", action="store_true", help="print the random-row bandwidth ceilings and exit")
     ap.add_argument("--probe-gb", type=int, default=32)
     ap.add_argument("--rows", type=int, default=0, help="override R (reduced case for profiling)")

@@ -101,6 +101,13 @@ def lib():
                 [C, P, P, i64, i32, i64, P, P, P, P, P, i64, P, sz, P, P, P, P, P],
                 ctypes.c_int,
             ),
+            "engram_host_alloc": ([sz, ctypes.POINTER(P)], ctypes.c_int),
+            "engram_host_free": ([P], ctypes.c_int),
+            "engram_forward_host_pipelined_workspace_bytes": ([C, i64, i64, i64], sz),
+            "engram_forward_host_pipelined": (
+                [C, P, P, i64, i32, i64, P, P, P, P, P, i64, i64, P, sz, P, P, P, ctypes.POINTER(P)],
+                ctypes.c_int,
+            ),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -223,6 +230,72 @@ def engram_forward(cfg, tokens, seq_offsets, tables, scales, W_out, g, h, last_n
         "engram_forward",
     )
     return h
+
+
+def host_tables_empty(shape, dtype=torch.uint8):
+    """A CPU tensor in pinned host memory on transparent huge pages (zeroed),
+    from engram_host_alloc.  The tensor's storage holds the buffer object, so
+    the memory is released once the last tensor or view of it is gone."""
+    n = 1
+    for x in shape:
+        n *= int(x)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    ptr = ctypes.c_void_p()
+    _check(lib().engram_host_alloc(nbytes, ctypes.byref(ptr)), "engram_host_alloc")
+
+    class _HostBuffer(ctypes.c_uint8 * nbytes):
+        def __del__(self):
+            lib().engram_host_free(ctypes.c_void_p(ctypes.addressof(self)))
+
+    buf = _HostBuffer.from_address(ptr.value)
+    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype).view(*shape)
+
+
+def engram_forward_host_pipelined_workspace_bytes(cfg, n_query, chunk, capacity):
+    return int(lib().engram_forward_host_pipelined_workspace_bytes(ctypes.byref(cfg), int(n_query), int(chunk),
+                                                                   int(capacity)))
+
+
+def engram_forward_host_pipelined(cfg, tokens, seq_offsets, host_tables, host_scales, W_out, g, h, chunk,
+                                  capacity=None, last_n=0, n_query=None, workspace=None, n_unique=None, stream=None,
+                                  side_stream=None, events=None):
+    """The host-table path in chunks of `chunk` query tokens: chunk k+1's dedup
+    and staging overlap chunk k's gather; one projection follows.  Returns
+    n_unique (int64 per chunk).  `capacity` defaults to chunk * 48 rows per
+    staging set."""
+    _need(tokens, torch.int32, "tokens")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(host_tables, torch.uint8, "host_tables", cuda=False)
+    _need(host_scales, torch.float32, "host_scales", cuda=False)
+    _need(h, torch.bfloat16, "h")
+    nq = _n_query(tokens, seq_offsets, last_n, n_query)
+    dev = h.device
+    chunk = int(min(chunk, max(nq, 1)))
+    if capacity is None:
+        capacity = chunk * N_TABLES
+    if workspace is None:
+        workspace = torch.empty(engram_forward_host_pipelined_workspace_bytes(cfg, nq, chunk, capacity),
+                                dtype=torch.uint8, device=dev)
+    n_chunks = max(1, -(-nq // chunk))
+    if n_unique is None:
+        n_unique = torch.zeros(n_chunks, dtype=torch.int64, device=dev)
+    if side_stream is None:
+        side_stream = torch.cuda.Stream(device=dev)
+    if events is None:
+        events = [torch.cuda.Event() for _ in range(6)]
+    for ev in events:  # make sure the events exist as CUDA events before passing their handles
+        if ev.cuda_event == 0:
+            ev.record(torch.cuda.current_stream() if stream is None else stream)
+    handles = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
+    _check(
+        lib().engram_forward_host_pipelined(
+            ctypes.byref(cfg), _ptr(tokens), _ptr(seq_offsets), seq_offsets.numel() - 1, last_n, nq,
+            _ptr(host_tables), _ptr(host_scales), _ptr(W_out), _ptr(g), _ptr(h), chunk, int(capacity),
+            _ptr(workspace), workspace.numel(), _ptr(n_unique), _stream(stream),
+            ctypes.c_void_p(side_stream.cuda_stream), handles),
+        "engram_forward_host_pipelined",
+    )
+    return n_unique
 
 
 NO_WORKSPACE_MAX_QUERY = 16384

@@ -8,8 +8,11 @@
 // the table that is never multiplied" (suffix n-grams, one row per (order,
 // head), 256-byte FP8 rows, host tables read over unified addressing on a
 // side stream, bitwise-identical host-table mode).
+#include <sys/mman.h>
+
 #include <algorithm>
 #include <cstdio>
+#include <map>
 #include <mutex>
 #include <cstdlib>
 #include <cstring>
@@ -760,8 +763,10 @@ static int pick_cpg_h_resident(int64_t m_tiles, int n_chunks) {
 
 // y = X @ W_out and the gated residual update.  X comes either from fp32 mem
 // (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
+// split_tiles > 0: choose the kernel and the split of d as for a batch of
+// split_tiles tiles (a chunk of a larger batch then gives that batch's bits).
 engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint16_t *x_bf16, const uint16_t *W,
-                          const uint16_t *g, uint16_t *h, int64_t n_query, cudaStream_t st) {
+                          const uint16_t *g, uint16_t *h, int64_t n_query, cudaStream_t st, int64_t split_tiles = 0) {
     const int d = cfg->d_model;
     const int n_chunks = d / fuse::BN;
     fuse::Params p;
@@ -772,8 +777,9 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     p.m_tiles = (n_query + fuse::BM - 1) / fuse::BM;
     p.d = d;
     // One split of d for both inputs (fp32 mem or bf16 X), so they agree bit for bit.
-    const int cpg3 = pick_cpg_h_resident(p.m_tiles, n_chunks);
-    p.groups = cpg3 ? n_chunks / cpg3 : pick_groups(p.m_tiles, n_chunks);
+    const int64_t tiles_for_split = split_tiles > 0 ? split_tiles : p.m_tiles;
+    const int cpg3 = pick_cpg_h_resident(tiles_for_split, n_chunks);
+    p.groups = cpg3 ? n_chunks / cpg3 : pick_groups(tiles_for_split, n_chunks);
     if (p.groups == 0) return ENGRAM_EINVAL;
     p.cpg = n_chunks / p.groups;
     p.eps = cfg->rms_eps;
@@ -1024,6 +1030,173 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
                       nullptr, n_query, capacity, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
+}
+
+// ========================================================= host tables ====
+// Pinned host memory for tables read by the device over the host link,
+// backed by transparent huge pages where the kernel offers them.  Staging
+// touches rows scattered over tens of GB; with base pages (64 KB on this
+// class of host) the device spends much of its time translating addresses.
+
+static std::mutex g_host_mu;
+static std::map<void *, std::pair<void *, size_t>> g_host_maps;  // aligned pointer -> mapping
+
+static size_t huge_page_bytes() {
+    size_t v = 0;
+    if (FILE *f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long x = 0;
+        if (fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+        fclose(f);
+    }
+    return (v >= 4096 && (v & (v - 1)) == 0) ? v : (size_t)2 << 20;
+}
+
+extern "C" engram_status engram_host_alloc(size_t bytes, void **ptr) {
+    if (!ptr) return ENGRAM_EINVAL;
+    *ptr = nullptr;
+    if (bytes == 0) return ENGRAM_EINVAL;
+    const size_t align = huge_page_bytes();
+    const size_t len = (bytes + align - 1) / align * align + align;
+    void *raw = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (raw == MAP_FAILED) return ENGRAM_ENOMEM;
+    void *p = reinterpret_cast<void *>((reinterpret_cast<uintptr_t>(raw) + align - 1) / align * align);
+    const size_t plen = (bytes + align - 1) / align * align;
+    madvise(p, plen, MADV_HUGEPAGE);  // a hint: plain pages if the kernel declines
+    const cudaError_t e = cudaHostRegister(p, plen, cudaHostRegisterDefault);
+    if (e != cudaSuccess) {
+        munmap(raw, len);
+        return cuda_fail(e, "cudaHostRegister");
+    }
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    g_host_maps[p] = {raw, len};
+    *ptr = p;
+    return ENGRAM_OK;
+}
+
+extern "C" engram_status engram_host_free(void *ptr) {
+    if (!ptr) return ENGRAM_OK;
+    std::pair<void *, size_t> m;
+    {
+        std::lock_guard<std::mutex> lock(g_host_mu);
+        auto it = g_host_maps.find(ptr);
+        if (it == g_host_maps.end()) return ENGRAM_EINVAL;
+        m = it->second;
+        g_host_maps.erase(it);
+    }
+    const cudaError_t e = cudaHostUnregister(ptr);
+    munmap(m.first, m.second);
+    return e == cudaSuccess ? ENGRAM_OK : cuda_fail(e, "cudaHostUnregister");
+}
+
+// ================================================== pipelined host path ====
+// Workspace: idx [n][48] i64 | X [n][512] bf16 | two staging sets, each
+// idx_staged [chunk][48] i32 | unique [cap] i64 | rows [cap][stride] |
+// scales [cap] f32 | dedup workspace.
+struct PipeLayout {
+    size_t idx, x, set[2], set_bytes, idx_staged, unique, rows, scales, dedup, total;
+};
+
+static PipeLayout pipe_layout(const engram_config *cfg, int64_t n_query, int64_t chunk, int64_t capacity) {
+    PipeLayout L;
+    size_t o = 0;
+    L.idx = o;
+    o += round_up((size_t)n_query * kTables * 8, 256);
+    L.x = o;
+    o += round_up((size_t)n_query * kMem * 2, 256);
+    L.idx_staged = 0;  // offsets inside a staging set
+    L.unique = round_up((size_t)chunk * kTables * 4, 256);
+    L.rows = L.unique + round_up((size_t)capacity * 8, 256);
+    L.scales = L.rows + round_up((size_t)capacity * staged_stride(cfg), 256);
+    L.set_bytes = L.scales + round_up((size_t)capacity * 4, 256);
+    L.set[0] = o;
+    o += L.set_bytes;
+    L.set[1] = o;
+    o += L.set_bytes;
+    L.dedup = o;
+    o += dedup_bytes(cfg);
+    L.total = o;
+    return L;
+}
+
+extern "C" size_t engram_forward_host_pipelined_workspace_bytes(const engram_config *cfg, int64_t n_query,
+                                                                int64_t chunk, int64_t capacity) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || chunk < 1 || capacity < 1) return 0;
+    return pipe_layout(cfg, n_query, chunk, capacity).total;
+}
+
+extern "C" engram_status engram_forward_host_pipelined(const engram_config *cfg, const int32_t *tokens,
+                                                       const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                                       int64_t n_query, const uint8_t *host_tables,
+                                                       const float *host_scales, const uint16_t *W_out,
+                                                       const uint16_t *g, uint16_t *h, int64_t chunk, int64_t capacity,
+                                                       void *workspace, size_t workspace_bytes, int64_t *n_unique,
+                                                       void *stream, void *side_stream, void *const *events) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0 || chunk < 1 || capacity < 1)
+        return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !host_tables || !scales_ok(cfg, host_scales) || !workspace ||
+        !n_unique || !events)
+        return ENGRAM_EINVAL;
+    for (int e = 0; e < 6; ++e)
+        if (!events[e]) return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
+    if (!aligned(host_tables, 16) || !aligned(workspace, 256) || !aligned(n_unique, 8)) return ENGRAM_EINVAL;
+    if (n_query * kTables >= (INT64_C(1) << 31) || capacity >= (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    chunk = std::min(chunk, n_query);
+    const PipeLayout L = pipe_layout(cfg, n_query, chunk, capacity);
+    if (workspace_bytes < L.total) return ENGRAM_ENOMEM;
+    cudaStream_t st = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
+    cudaEvent_t ev_dedup[2] = {(cudaEvent_t)events[0], (cudaEvent_t)events[1]};
+    cudaEvent_t ev_staged[2] = {(cudaEvent_t)events[2], (cudaEvent_t)events[3]};
+    cudaEvent_t ev_used[2] = {(cudaEvent_t)events[4], (cudaEvent_t)events[5]};
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int64_t *idx = reinterpret_cast<int64_t *>(ws + L.idx);
+    uint16_t *X = reinterpret_cast<uint16_t *>(ws + L.x);
+    void *dws = ws + L.dedup;
+    auto set_idx_staged = [&](int b) { return reinterpret_cast<int32_t *>(ws + L.set[b] + L.idx_staged); };
+    auto set_unique = [&](int b) { return reinterpret_cast<int64_t *>(ws + L.set[b] + L.unique); };
+    auto set_rows = [&](int b) { return ws + L.set[b] + L.rows; };
+    auto set_scales = [&](int b) { return reinterpret_cast<float *>(ws + L.set[b] + L.scales); };
+    const int64_t n_chunks = (n_query + chunk - 1) / chunk;
+    const int64_t all_tiles = (n_query + fuse::BM - 1) / fuse::BM;
+
+    engram_status s = hash_launch(cfg, tokens, seq_offsets, n_seqs, last_n, n_query, idx, st);
+    if (s != ENGRAM_OK) return s;
+    // dedup (stream) then stage (side stream) of chunk k into staging set k & 1
+    auto issue = [&](int64_t k) -> engram_status {
+        const int b = (int)(k & 1);
+        const int64_t q0 = k * chunk, nk = std::min(chunk, n_query - q0);
+        engram_status r = dedup_launch(cfg, idx + q0 * kTables, nk, dws, set_unique(b), capacity, set_idx_staged(b),
+                                       n_unique + k, st);
+        if (r != ENGRAM_OK) return r;
+        if (cudaEventRecord(ev_dedup[b], st) != cudaSuccess) return ENGRAM_ECUDA;
+        if (cudaStreamWaitEvent(side, ev_dedup[b], 0) != cudaSuccess) return ENGRAM_ECUDA;
+        if (k >= 2 && cudaStreamWaitEvent(side, ev_used[b], 0) != cudaSuccess) return ENGRAM_ECUDA;
+        r = stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), mx(cfg), set_unique(b),
+                         n_unique + k, capacity, set_rows(b), set_scales(b), side);
+        if (r != ENGRAM_OK) return r;
+        return cudaEventRecord(ev_staged[b], side) == cudaSuccess ? ENGRAM_OK : ENGRAM_ECUDA;
+    };
+    s = issue(0);
+    if (s != ENGRAM_OK) return s;
+    for (int64_t k = 0; k < n_chunks; ++k) {
+        if (k + 1 < n_chunks) {  // the next chunk's dedup and staging run under this chunk's gather
+            s = issue(k + 1);
+            if (s != ENGRAM_OK) return s;
+        }
+        const int b = (int)(k & 1);
+        const int64_t q0 = k * chunk, nk = std::min(chunk, n_query - q0);
+        if (cudaStreamWaitEvent(st, ev_staged[b], 0) != cudaSuccess) return ENGRAM_ECUDA;
+        s = gather_launch(IDX_STAGED_I32, true, set_rows(b), mx(cfg) ? nullptr : set_scales(b), staged_stride(cfg),
+                          mx(cfg), set_idx_staged(b), nullptr, nk, capacity, X + q0 * kMem, st);
+        if (s != ENGRAM_OK) return s;
+        if (cudaEventRecord(ev_used[b], st) != cudaSuccess) return ENGRAM_ECUDA;
+    }
+    // One projection over the whole batch: the projection kernel is persistent
+    // (one cluster per group of SMs, striding over tiles), so it is not run
+    // beside a staging kernel that holds SMs.
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st, all_tiles);
 }
 
 // ====================================================== no-workspace variant ==

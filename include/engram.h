@@ -258,6 +258,56 @@ engram_status engram_forward_host(const engram_config *cfg, const int32_t *token
                                   int64_t *n_unique, void *stream, void *side_stream, void *ev_dedup,
                                   void *ev_staged);
 
+/*
+ * The host-table path pipelined over chunks of `chunk` query tokens (the
+ * pages' background prefetch of host rows on a side stream, "Engram: the table
+ * that is never multiplied", applied chunk by chunk).  All queries are hashed
+ * first; then, for chunk k, the unique rows are found on `stream` and staged
+ * on `side_stream` into one of two staging sets (k mod 2), and the staged
+ * gather of chunk k runs on `stream` while chunk k+1 is being deduplicated and
+ * staged; one projection over the whole batch follows.  h equals
+ * engram_forward's on the same tables bit for bit.  Rows used by several
+ * chunks cross the host link once per chunk.
+ *   chunk       query tokens per chunk (>= 1; a multiple of 128 keeps whole
+ *               tiles per chunk)
+ *   capacity    staging rows per set; at least the unique rows of any chunk
+ *               (chunk * 48 always suffices); more raise ENGRAM_ECAPACITY
+ *   n_unique    int64 [ceil(n_query / chunk)] (device): unique rows per chunk
+ *   events      6 caller-created events (cudaEventDisableTiming is fine):
+ *               dedup done x2, staged x2, staging set consumed x2
+ * workspace >= engram_forward_host_pipelined_workspace_bytes(cfg, n_query,
+ * chunk, capacity); host tables and scales as in engram_forward_host.
+ * Argument errors return synchronously; device-side range and capacity errors
+ * set the sticky error word.
+ */
+/*
+ * Pinned host memory for host tables (engram_stage, engram_forward_host,
+ * engram_forward_host_pipelined), mapped on transparent huge pages where the
+ * operating system offers them and registered with the CUDA driver, so the
+ * device reaches it through unified addressing (the pages' host-resident
+ * tables read over the host link, "Engram: the table that is never
+ * multiplied").  Staging reads rows scattered over tens of GB; with base pages
+ * the device spends much of that time translating addresses.  This is the one
+ * call that allocates; it is host-only and synchronous.
+ *   engram_host_alloc: *ptr receives `bytes` of zeroed, pinned memory aligned
+ *   to the huge page size; ENGRAM_EINVAL for bytes == 0 or ptr == NULL,
+ *   ENGRAM_ENOMEM if the mapping fails, ENGRAM_ECUDA if registration fails.
+ *   engram_host_free: releases a pointer from engram_host_alloc (NULL is a
+ *   no-op; any other pointer is ENGRAM_EINVAL); no device work may still use it.
+ */
+engram_status engram_host_alloc(size_t bytes, void **ptr);
+engram_status engram_host_free(void *ptr);
+
+size_t engram_forward_host_pipelined_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t chunk,
+                                                     int64_t capacity);
+engram_status engram_forward_host_pipelined(const engram_config *cfg, const int32_t *tokens,
+                                            const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                            int64_t n_query, const uint8_t *host_tables, const float *host_scales,
+                                            const uint16_t *W_out, const uint16_t *g, uint16_t *h, int64_t chunk,
+                                            int64_t capacity, void *workspace, size_t workspace_bytes,
+                                            int64_t *n_unique, void *stream, void *side_stream,
+                                            void *const *events);
+
 #ifdef __cplusplus
 }
 #endif

@@ -56,6 +56,10 @@ def test_workspace_sizes(eg):
     d = eg.engram_dedup_workspace_bytes(c)
     assert d >= 2 * 48 * cfg.R // 32 * 4
     assert eg.engram_forward_host_workspace_bytes(c, 100, 4800) >= 4800 * 256
+    # the pipelined host path: two staging sets, each sized by the chunk
+    p1 = eg.engram_forward_host_pipelined_workspace_bytes(c, 65536, 8192, 8192 * 48)
+    p2 = eg.engram_forward_host_pipelined_workspace_bytes(c, 65536, 16384, 16384 * 48)
+    assert p2 - p1 >= 2 * 8192 * 48 * 256 and eg.engram_forward_host_pipelined_workspace_bytes(c, 100, 0, 10) == 0
     # MX rows are staged whole: 272 bytes a staged row
     cm = eg.make_config(cfg.V, cfg.R, cfg.d, default_seeds(), row_layout=eg.ROWS_MX)
     assert eg.engram_forward_host_workspace_bytes(cm, 100, 4800) >= 4800 * 272
@@ -80,6 +84,22 @@ def test_invalid_arguments_rejected_before_any_device_work(eg):
     c3 = eg.make_config(1024, 0, 256, default_seeds())
     assert lib.engram_gather_reduce(ctypes.byref(c3), ctypes.c_void_p(256), ctypes.c_void_p(256),
                                     ctypes.c_void_p(256), 4, ctypes.c_void_p(256), null) == 1
+    # pipelined host path: chunk < 1, null events
+    ev6 = (ctypes.c_void_p * 6)(*([256] * 6))
+    assert lib.engram_forward_host_pipelined(ctypes.byref(c), ctypes.c_void_p(256), ctypes.c_void_p(256), 1, 0, 4,
+                                             ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                                             ctypes.c_void_p(256), ctypes.c_void_p(256), 0, 64,
+                                             ctypes.c_void_p(256), 1 << 30, ctypes.c_void_p(256), null, null,
+                                             ev6) == 1
+    assert lib.engram_forward_host_pipelined(ctypes.byref(c), ctypes.c_void_p(256), ctypes.c_void_p(256), 1, 0, 4,
+                                             ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                                             ctypes.c_void_p(256), ctypes.c_void_p(256), 4, 64,
+                                             ctypes.c_void_p(256), 1 << 30, ctypes.c_void_p(256), null, null,
+                                             None) == 1
+    # host table allocator: zero bytes or a null out-pointer; freeing a foreign pointer
+    out = ctypes.c_void_p()
+    assert lib.engram_host_alloc(0, ctypes.byref(out)) == 1 and lib.engram_host_alloc(64, None) == 1
+    assert lib.engram_host_free(ctypes.c_void_p(4096)) == 1 and lib.engram_host_free(None) == 0
     # unknown row layout
     c4 = eg.make_config(1024, 4096, 256, default_seeds(), row_layout=3)
     assert lib.engram_gather_reduce(ctypes.byref(c4), ctypes.c_void_p(256), ctypes.c_void_p(256),

@@ -134,6 +134,76 @@ def test_host_path_mx_layout(eg):
     check_h(hb[torch.from_numpy(q).cuda()], ref_h)
 
 
+@pytest.mark.parametrize("chunk", [128, 384, 1000, 4096])
+def test_host_pipelined_bit_identical_to_hbm(eg, chunk):
+    """The chunked, pipelined host path gives the HBM forward's h bits, and
+    each chunk stages exactly its own distinct rows."""
+    w = Workload(SMALL_HOST, host_tables=True)
+    cfg = w.cfg
+    h_pipe = w.fresh_h()
+    n_unique = eg.engram_forward_host_pipelined(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h_pipe,
+                                                chunk=chunk)
+    dev_tables, dev_scales = w.tables.cuda(), w.scales.cuda()
+    h_hbm = w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, dev_tables, dev_scales, w.W, w.g, h_hbm)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_pipe.view(torch.int16), h_hbm.view(torch.int16))
+    ref_idx = w.ref_idx_all()
+    c = min(chunk, cfg.tq)
+    want = [len(_unique_ref(ref_idx[q0:q0 + c], cfg.R)) for q0 in range(0, cfg.tq, c)]
+    assert n_unique.cpu().tolist() == want
+
+
+def test_host_pipelined_many_tiles_and_mx(eg):
+    """83 tiles in chunks of 16 tiles: every chunk's projection splits d as for
+    the whole batch (the many-tile kernel), so h keeps the HBM path's bits; and
+    MXFP8-style rows through the same pipeline."""
+    cfg = CONFIGS["host"].with_(seq_lens=(6000, 4500), R=1 << 16, seed=12)
+    w = Workload(cfg, host_tables=True)
+    h_pipe, h_hbm = w.fresh_h(), w.fresh_h()
+    eg.engram_forward_host_pipelined(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h_pipe, chunk=2048)
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables.cuda(), w.scales.cuda(), w.W, w.g, h_hbm)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_pipe.view(torch.int16), h_hbm.view(torch.int16))
+    del w
+    m = Workload(SMALL_HOST, host_tables=True, layout="mx")
+    h_pipe, h_hbm = m.fresh_h(), m.fresh_h()
+    eg.engram_forward_host_pipelined(m.c, m.tokens, m.seq_offsets, m.tables, None, m.W, m.g, h_pipe, chunk=384)
+    eg.engram_forward(m.c, m.tokens, m.seq_offsets, m.tables.cuda(), None, m.W, m.g, h_hbm)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_pipe.view(torch.int16), h_hbm.view(torch.int16))
+
+
+def test_host_tables_on_huge_pages(eg):
+    """Tables in engram_host_alloc memory (pinned, transparent huge pages):
+    staged bytes equal the table rows, and the host-table forward gives the
+    HBM forward's bits."""
+    w = Workload(SMALL_HOST, host_tables=True)
+    t = eg.host_tables_empty(tuple(w.tables.shape), torch.uint8)
+    s = eg.host_tables_empty(tuple(w.scales.shape), torch.float32)
+    assert t.is_pinned() and s.is_pinned() and t.data_ptr() % 4096 == 0
+    t.copy_(w.tables)
+    s.copy_(w.scales)
+    cap = w.cfg.tq * 48
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    unique, idx_staged, n_unique = eg.engram_dedup(w.c, idx, cap)
+    rows, scales = eg.engram_stage(w.c, t, s, unique, n_unique, cap)
+    h1, h2 = w.fresh_h(), w.fresh_h()
+    eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, t, s, w.W, w.g, h1, capacity=cap)
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables.cuda(), w.scales.cuda(), w.W, w.g, h2)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    U = int(n_unique.item())
+    u = unique[:U].cpu()
+    assert torch.equal(rows[:U].cpu(), w.tables.view(-1, 256)[u])
+    assert torch.equal(scales[:U].cpu(), w.scales.view(-1)[u])
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    del t, s
+
+
 def test_host_path_full_size(eg):
     """The host-table workload at full size (51.5 GB of pinned tables)."""
     cfg = CONFIGS["host"]
