@@ -270,3 +270,86 @@ int orc_fuse(const double *mem, const uint16_t *W, const uint16_t *g, uint16_t *
     free(y);
     return ORC_OK;
 }
+
+/*
+ * One Engram layer with a per-row, content-aware gate (rohitghumare.com
+ * "guides/deepseek-v4-1-flash": section "The architecture", two layers, 1 and
+ * 14, each adding looked-up rows into the residual stream through a learned
+ * gate; section "Engram: the table that is never multiplied", 24 rows per
+ * Engram layer and a gate that compares each retrieved row with the hidden
+ * state and suppresses it when it contradicts the context).
+ *
+ * The pages give no gate formula; this is the plainest one that matches the
+ * description (a reading, listed in the design notes): for each of the
+ * layer's 24 rows r_j (dequantized, scale times e4m3 value),
+ *   q   = rmsnorm(h) W_q            (W_q: d x 256)
+ *   k_j = rmsnorm(r_j) W_k          (W_k: 256 x 256)
+ *   g_j = sigmoid(<q, k_j> / sqrt(256))
+ *   e   = sum_j g_j r_j             (in table order j)
+ *   X   = bf16(e);  y = X W_m       (W_m: 256 x d)
+ *   h   = bf16(h + y)
+ * rmsnorm(v) = v / sqrt(mean(v^2) + eps), without a weight.  All sums in
+ * double; weights and h are bf16 bit patterns.
+ *
+ * codes: e4m3 [T][24][256]; scales: fp32 [T][24]; h: bf16 [T][d], updated in
+ * place; gates (optional): [T][24] out; e_out (optional): [T][256] out.
+ */
+int orc_layer_gated(const uint8_t *codes, const float *scales, const uint16_t *Wq, const uint16_t *Wk,
+                    const uint16_t *Wm, uint16_t *h, int64_t T, int32_t d, double eps, double *gates,
+                    double *e_out) {
+    enum { R = 256, J = 24 };
+    if (d <= 0) return ORC_EINVAL;
+    double *q = (double *)malloc(sizeof(double) * R);
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    double *hv = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!q || !y || !hv) {
+        free(q);
+        free(y);
+        free(hv);
+        return ORC_EINVAL;
+    }
+    double v[R], k[R], e[R], X[R];
+    for (int64_t t = 0; t < T; ++t) {
+        uint16_t *ht = h + t * (int64_t)d;
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) {
+            hv[i] = orc_bf16_value(ht[i]);
+            ss += hv[i] * hv[i];
+        }
+        const double rh = 1.0 / sqrt(ss / (double)d + eps);
+        for (int c = 0; c < R; ++c) q[c] = 0.0;
+        for (int i = 0; i < d; ++i)
+            for (int c = 0; c < R; ++c) q[c] += (hv[i] * rh) * orc_bf16_value(Wq[(int64_t)i * R + c]);
+        for (int c = 0; c < R; ++c) e[c] = 0.0;
+        for (int j = 0; j < J; ++j) {
+            const uint8_t *row = codes + (t * J + j) * R;
+            const double s = (double)scales[t * J + j];
+            double vs = 0.0;
+            for (int c = 0; c < R; ++c) {
+                v[c] = s * orc_e4m3_value(row[c]);
+                vs += v[c] * v[c];
+            }
+            const double rr = 1.0 / sqrt(vs / (double)R + eps);
+            for (int c = 0; c < R; ++c) k[c] = 0.0;
+            for (int i = 0; i < R; ++i)
+                for (int c = 0; c < R; ++c) k[c] += (v[i] * rr) * orc_bf16_value(Wk[i * R + c]);
+            double score = 0.0;
+            for (int c = 0; c < R; ++c) score += q[c] * k[c];
+            const double g = 1.0 / (1.0 + exp(-score / sqrt((double)R)));
+            if (gates) gates[t * J + j] = g;
+            for (int c = 0; c < R; ++c) e[c] += g * v[c];
+        }
+        for (int c = 0; c < R; ++c) {
+            if (e_out) e_out[t * R + c] = e[c];
+            X[c] = orc_bf16_value(orc_bf16_rne(e[c]));
+        }
+        for (int n = 0; n < d; ++n) y[n] = 0.0;
+        for (int c = 0; c < R; ++c)
+            for (int n = 0; n < d; ++n) y[n] += X[c] * orc_bf16_value(Wm[(int64_t)c * d + n]);
+        for (int n = 0; n < d; ++n) ht[n] = orc_bf16_rne(hv[n] + y[n]);
+    }
+    free(q);
+    free(y);
+    free(hv);
+    return ORC_OK;
+}

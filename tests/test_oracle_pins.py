@@ -481,3 +481,95 @@ def test_page_figures_from_oracle_accounting():
     assert round(2000 * with_scales / 1e6) == fig["host_traffic_2000tps"][0]  # 25.3 MB/s
     assert round(131072 * with_scales / 1e9, 1) == fig["prompt_128k_reads"][0]  # 1.66 GB
     assert fig["modules"][0] * 3 * fig["heads_per_order"][0] == rows
+
+
+# ----------------------------------------------- per-row gated Engram layer --
+
+def _bf16_bits(x):
+    """float64 array -> bf16 bit patterns (torch's round-to-nearest-even)."""
+    return torch.from_numpy(np.asarray(x, np.float64)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_vals(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _e4m3_vals(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _layer_inputs(T=3, d=256, seed=41):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, (T, 24, 256)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    scales = rng.uniform(0.5, 2.0, (T, 24)).astype(np.float32)
+    Wq = _bf16_bits(rng.standard_normal((d, 256)) / np.sqrt(d))
+    Wk = _bf16_bits(rng.standard_normal((256, 256)) / 16.0)
+    Wm = _bf16_bits(rng.standard_normal((256, d)) / 16.0)
+    h = _bf16_bits(rng.standard_normal((T, d)))
+    return codes, scales, Wq, Wk, Wm, h
+
+
+def test_layer_gate_half_when_query_is_zero():
+    """W_q = 0: every score is 0, every gate exactly 1/2, e is half the plain
+    module sum (torch's decoder), and with W_m = I (d = 256) h becomes
+    bf16(h + bf16(e)) (torch's rounding)."""
+    codes, scales, Wq, Wk, Wm, h = _layer_inputs()
+    Wq = np.zeros_like(Wq)
+    eye = _bf16_bits(np.eye(256))
+    hn, gates, e = oracle.layer_gated(codes, scales, Wq, Wk, eye, h)
+    assert np.all(gates == 0.5)
+    plain = (_e4m3_vals(codes) * scales[:, :, None].astype(np.float64)).sum(axis=1)
+    assert np.array_equal(e, plain / 2)
+    X = _bf16_vals(_bf16_bits(e))
+    assert np.array_equal(hn, _bf16_bits(_bf16_vals(h) + X))
+
+
+def test_layer_zero_projection_leaves_h():
+    codes, scales, Wq, Wk, Wm, h = _layer_inputs(d=512)
+    hn, _, _ = oracle.layer_gated(codes, scales, Wq, Wk, np.zeros_like(Wm), h)
+    assert np.array_equal(hn, h)
+
+
+def test_layer_closed_form_scores():
+    """Constant h and constant rows with eps = 0: rmsnorm gives +-1 vectors, and
+    with W_q (2^-9, d = 512) and W_k (2^-8) one-hot in column 0 every dot is
+    sign(h) * sign(row) exactly, so each gate is sigmoid(+-1/16): the score is
+    divided by sqrt(256), the width of the dot, not by sqrt(d)."""
+    T, d = 2, 512
+    rng = np.random.default_rng(5)
+    codes = np.zeros((T, 24, 256), np.uint8)
+    pick = rng.choice(np.array([0x38, 0x40, 0xB8, 0xC4, 0x2A, 0xAA], np.uint8), (T, 24))
+    codes[:] = pick[:, :, None]
+    scales = rng.uniform(0.5, 2.0, (T, 24)).astype(np.float32)
+    Wq = np.zeros((d, 256), np.uint16)
+    Wq[:, 0] = _bf16_bits(np.full(d, 2.0**-9))
+    Wk = np.zeros((256, 256), np.uint16)
+    Wk[:, 0] = _bf16_bits(np.full(256, 2.0**-8))
+    hsign = np.array([1.0, -1.0])
+    h = _bf16_bits(np.repeat(hsign[:, None] * 0.75, d, axis=1))
+    _, gates, e = oracle.layer_gated(codes, scales, Wq, Wk, np.zeros((256, d), np.uint16), h, eps=0.0)
+    vals = _e4m3_vals(pick) * scales.astype(np.float64)
+    want = 1.0 / (1.0 + np.exp(-(hsign[:, None] * np.sign(vals)) / 16.0))
+    assert np.allclose(gates, want, rtol=0, atol=1e-15)
+    assert np.allclose(e, (want * vals).sum(axis=1)[:, None] * np.ones(256), rtol=1e-14, atol=0)
+
+
+def test_layer_gate_symmetries():
+    """Negating W_k turns every gate g into 1 - g; permuting a token's rows
+    permutes its gates and leaves e unchanged; doubling one row's scale leaves
+    its gate (rmsnorm, eps = 0) and adds exactly g_j * r_j to e."""
+    codes, scales, Wq, Wk, Wm, h = _layer_inputs(T=2, d=256)
+    _, g1, e1 = oracle.layer_gated(codes, scales, Wq, Wk, Wm, h, eps=0.0)
+    _, g2, _ = oracle.layer_gated(codes, scales, Wq, Wk ^ np.uint16(0x8000), Wm, h, eps=0.0)
+    assert np.allclose(g1 + g2, 1.0, rtol=0, atol=1e-14)
+    perm = np.random.default_rng(3).permutation(24)
+    _, g3, e3 = oracle.layer_gated(codes[:, perm], scales[:, perm], Wq, Wk, Wm, h, eps=0.0)
+    assert np.allclose(g3, g1[:, perm], rtol=0, atol=1e-15)
+    assert np.allclose(e3, e1, rtol=1e-13, atol=1e-13)
+    s2 = scales.copy()
+    s2[:, 7] *= 2
+    _, g4, e4 = oracle.layer_gated(codes, s2, Wq, Wk, Wm, h, eps=0.0)
+    assert np.allclose(g4, g1, rtol=0, atol=1e-15)
+    r7 = _e4m3_vals(codes[:, 7]) * scales[:, 7:8].astype(np.float64)
+    assert np.allclose(e4 - e1, g1[:, 7:8] * r7, rtol=1e-12, atol=1e-12)
