@@ -101,6 +101,9 @@ def lib():
                 [C, P, P, i64, i32, i64, P, P, P, P, P, i64, P, sz, P, P, P, P, P],
                 ctypes.c_int,
             ),
+            "engram_layer_keys": ([C, P, P, P], ctypes.c_int),
+            "engram_layer_workspace_bytes": ([C, i64], sz),
+            "engram_layer_forward": ([C, i32, P, P, i64, i32, i64, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "engram_host_alloc": ([sz, ctypes.POINTER(P)], ctypes.c_int),
             "engram_host_free": ([P], ctypes.c_int),
             "engram_forward_host_pipelined_workspace_bytes": ([C, i64, i64, i64], sz),
@@ -230,6 +233,62 @@ def engram_forward(cfg, tokens, seq_offsets, tables, scales, W_out, g, h, last_n
         "engram_forward",
     )
     return h
+
+
+LAYER_WIDTH = 256
+
+
+def engram_layer_keys(cfg, W_k, W_kk=None, stream=None):
+    """W_kk [512,256] = [W_k^T ; W_k^T] for the per-row gates of one Engram layer."""
+    _need(W_k, torch.bfloat16, "W_k")
+    if W_kk is None:
+        W_kk = torch.empty((2 * LAYER_WIDTH, LAYER_WIDTH), dtype=torch.bfloat16, device=W_k.device)
+    _check(lib().engram_layer_keys(ctypes.byref(cfg), _ptr(W_k), _ptr(W_kk), _stream(stream)), "engram_layer_keys")
+    return W_kk
+
+
+def engram_layer_workspace_bytes(cfg, n_query):
+    return int(lib().engram_layer_workspace_bytes(ctypes.byref(cfg), int(n_query)))
+
+
+def engram_layer_forward(cfg, module, tokens, seq_offsets, tables, scales, W_q, W_kk, W_m, h, last_n=0,
+                         n_query=None, workspace=None, stream=None):
+    """One Engram layer (module 0 or 1) with per-row gates, in place on h."""
+    _need(tokens, torch.int32, "tokens")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(tables, torch.uint8, "tables")
+    _need(scales, torch.float32, "scales")
+    _need(W_q, torch.bfloat16, "W_q")
+    _need(W_kk, torch.bfloat16, "W_kk")
+    _need(W_m, torch.bfloat16, "W_m")
+    _need(h, torch.bfloat16, "h")
+    nq = _n_query(tokens, seq_offsets, last_n, n_query)
+    if workspace is None:
+        workspace = torch.empty(max(engram_layer_workspace_bytes(cfg, nq), 1), dtype=torch.uint8, device=h.device)
+    _need(workspace, torch.uint8, "workspace")
+    _check(
+        lib().engram_layer_forward(ctypes.byref(cfg), int(module), _ptr(tokens), _ptr(seq_offsets),
+                                   seq_offsets.numel() - 1, last_n, nq, _ptr(tables), _ptr(scales), _ptr(W_q),
+                                   _ptr(W_kk), _ptr(W_m), _ptr(h), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)),
+        "engram_layer_forward",
+    )
+    return h
+
+
+def layer_workspace_views(workspace, n_query):
+    """(q pair bf16 [n,512] = [q_hi | q_lo], u fp32 [n,256], X bf16 [n,256]) views
+    of an engram_layer_forward workspace."""
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    n, w = n_query, LAYER_WIDTH
+    ou = up(n * 2 * w * 2)
+    ox = ou + up(n * w * 4)
+    qp = workspace[: n * 2 * w * 2].view(torch.bfloat16).view(n, 2 * w)
+    u = workspace[ou: ou + n * w * 4].view(torch.float32).view(n, w)
+    X = workspace[ox: ox + n * w * 2].view(torch.bfloat16).view(n, w)
+    return qp, u, X
 
 
 def host_tables_empty(shape, dtype=torch.uint8):

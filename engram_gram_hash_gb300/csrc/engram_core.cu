@@ -23,6 +23,7 @@
 #include "fuse.cuh"
 #include "fuse2.cuh"
 #include "fuse3.cuh"
+#include "layer.cuh"
 
 namespace engram {
 
@@ -233,6 +234,128 @@ __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_c
         float *dst = static_cast<float *>(P.out) + col;
         reinterpret_cast<float4 *>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
         reinterpret_cast<float4 *>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+    }
+}
+
+// ============================================================ gated gather ==
+// One Engram layer's rows with per-row gates (the per-layer form): a warp per
+// query token reads the 24 rows of module m (tables 24m..24m+23, hashed in
+// place) and, for each row r_j (scale times e4m3 value), takes
+//   rr_j = 1 / sqrt(mean(r_j^2) + eps),   s_j = rr_j <q_t, r_j> / 16,
+//   g_j = sigmoid(s_j),                   X_t = bf16(sum_j g_j r_j)
+// against the token's key-side query u_t = rinv(h_t) h_t W_q W_k^T
+// (layer::query_kernel, twice).
+// Lane (half, c16) holds 16 values of rows 2i + half; a row's sums are reduced
+// over its half-warp; rows that failed the range check get gate 0.
+
+constexpr int kLayerWidth = 256;  // values per row: the width of one Engram layer's X and query
+
+struct GatedParams {
+    const uint8_t *rows;
+    const float *scales;  // fp32 [rows], or nullptr when each row carries its scale at byte 256
+    int64_t row_stride;
+    const float *q;       // [n_query][256]
+    uint16_t *X;          // [n_query][256] bf16 out
+    int64_t n_query;
+    int64_t R;
+    int32_t module;
+    float eps;
+    HashParams hp;
+};
+
+__global__ void __launch_bounds__(256, 2) gather_gated_kernel(const __grid_constant__ GatedParams P) {
+    __shared__ uint64_t s_seed[kTables];
+    if (threadIdx.x < kTables) s_seed[threadIdx.x] = P.hp.seeds[threadIdx.x];
+    if (blockIdx.x == 0 && threadIdx.x == 0 && P.hp.last_n == 0 &&
+        __ldg(P.hp.offs + P.hp.n_seqs) - __ldg(P.hp.offs) != P.hp.n_query)
+        raise_error(ENGRAM_ERANGE);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= P.n_query) return;
+
+    int64_t off = 0;
+    float sc = 0.f;
+    int ok = 0;
+    if (lane < kTablesPerModule) {
+        const int j = kTablesPerModule * P.module + lane;
+        int64_t start, pos;
+        bool bad = !query_position(P.hp, t, start, pos);
+        int64_t r = bad ? -1 : hash_one(P.hp, s_seed[j], j, start, pos, bad);
+        if (bad) r = -1;
+        ok = (r >= 0 && r < P.R);
+        if (!ok) raise_error(ENGRAM_ERANGE);
+        if (ok) {
+            const int64_t flat = (int64_t)j * P.R + r;
+            off = flat * P.row_stride;
+            sc = P.scales ? __ldg(P.scales + flat) : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
+        }
+    }
+    const int half = lane >> 4;
+    const int c16 = lane & 15;
+    float qv[16];
+    {
+        const float4 *qp = reinterpret_cast<const float4 *>(P.q + t * kLayerWidth + c16 * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 f = __ldg(qp + k);
+            qv[4 * k] = f.x;
+            qv[4 * k + 1] = f.y;
+            qv[4 * k + 2] = f.z;
+            qv[4 * k + 3] = f.w;
+        }
+    }
+    uint4 v[12];
+    float s[12];
+    uint32_t live = 0;  // bit i: row 2i + half passed the range check
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+        const int src = 2 * i + half;
+        const int64_t o = __shfl_sync(0xffffffffu, off, src);
+        s[i] = __shfl_sync(0xffffffffu, sc, src);
+        v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);
+        if (__shfl_sync(0xffffffffu, ok, src)) live |= 1u << i;
+    }
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+        float f[16];
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const float2 a = e4m3x2_to_float2((uint16_t)(w[q4] & 0xFFFFu));
+            const float2 b = e4m3x2_to_float2((uint16_t)(w[q4] >> 16));
+            f[4 * q4 + 0] = s[i] * a.x;
+            f[4 * q4 + 1] = s[i] * a.y;
+            f[4 * q4 + 2] = s[i] * b.x;
+            f[4 * q4 + 3] = s[i] * b.y;
+        }
+        float ss = 0.f, dd = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            ss = fmaf(f[k], f[k], ss);
+            dd = fmaf(f[k], qv[k], dd);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {  // over the 16 lanes of this half-warp
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            dd += __shfl_xor_sync(0xffffffffu, dd, o);
+        }
+        const float score = rsqrtf(ss * (1.f / 256.f) + P.eps) * dd * (1.f / 16.f);
+        const float g = (live >> i) & 1u ? 1.f / (1.f + __expf(-score)) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = fmaf(g, f[k], acc[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
+    if (half == 0) {
+        uint4 *dst = reinterpret_cast<uint4 *>(P.X + t * kLayerWidth + c16 * 16);
+        dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                            pack_bf16x2(acc[6], acc[7]));
+        dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                            pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
     }
 }
 
@@ -664,7 +787,7 @@ static int pick_groups(int64_t m_tiles, int n_chunks) {
 // X by TMA with the gate on its own warps (fuse2.cuh, many tiles); X by TMA
 // with the h slice held in shared memory (fuse3.cuh, few tiles: d slices of 1
 // or 2 chunks).  For the same split of d all three give the same bits.
-enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X_GATE_WARPS = 2 };
+enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X_GATE_WARPS = 2, FUSE_LAYER = 3 };
 
 // Persistent cluster launch: as many clusters of `groups` CTAs as fit at once
 // (cached per device and cluster size in *max_clusters), each striding over
@@ -714,6 +837,8 @@ template <int KIND, int CPG>
 static auto fuse_kernel_for() {
     if constexpr (KIND == FUSE_F32_MEM)
         return fuse::fuse_kernel<fuse::X_FROM_F32_MEM, CPG>;
+    else if constexpr (KIND == FUSE_LAYER)
+        return fuse2::fuse2_kernel<CPG, kLayerWidth / fuse::BK, false>;  // one layer's [T,256] X, no token gate
     else
         return fuse2::fuse2_kernel<CPG>;
 }
@@ -721,8 +846,9 @@ static auto fuse_kernel_for() {
 template <int KIND, int CPG>
 static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
                                    cudaStream_t st) {
-    constexpr int kThreads = KIND == FUSE_BF16_X_GATE_WARPS ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
-    constexpr int kSmem = KIND == FUSE_BF16_X_GATE_WARPS ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
+    constexpr bool k2 = KIND == FUSE_BF16_X_GATE_WARPS || KIND == FUSE_LAYER;
+    constexpr int kThreads = k2 ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
+    constexpr int kSmem = k2 ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
     static bool attr_done[64] = {};
     static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
     return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
@@ -803,6 +929,61 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
         return fuse_dispatch<FUSE_BF16_X_GATE_WARPS>(wmap, xmap, p, st);
     }
     return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, p, st);
+}
+
+// One Engram layer's projection: h = bf16(h + X W_m), X [n][256] bf16,
+// W_m [256][d] (fuse2 with 4 K-blocks and no token gate).
+static engram_status layer_projection_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W,
+                                             uint16_t *h, int64_t n_query, cudaStream_t st) {
+    const int d = cfg->d_model;
+    const int n_chunks = d / fuse::BN;
+    fuse::Params p;
+    memset(&p, 0, sizeof(p));
+    p.h = h;
+    p.n_query = n_query;
+    p.m_tiles = (n_query + fuse::BM - 1) / fuse::BM;
+    p.d = d;
+    p.groups = pick_groups(p.m_tiles, n_chunks);
+    if (p.groups == 0) return ENGRAM_EINVAL;
+    p.cpg = n_chunks / p.groups;
+    p.eps = cfg->rms_eps;
+    p.inv_sqrt_d = 1.0f / sqrtf((float)d);
+    CUtensorMap wmap, xmap;
+    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kLayerWidth, 64, fuse::BK)) return cuda_fail(cudaErrorInvalidValue, "W_m map");
+    if (!bf16_map_2d(&xmap, X, kLayerWidth, (uint64_t)n_query, fuse::BK, fuse::BM))
+        return cuda_fail(cudaErrorInvalidValue, "layer X map");
+    return fuse_dispatch<FUSE_LAYER>(wmap, xmap, p, st);
+}
+
+// out = s * (A @ B) on tcgen05 (layer::query_kernel): A bf16 [n][K], B bf16
+// [K][256]; with RMS s = rinv(A row), with SPLIT out is bf16 [n][512] (hi | lo)
+// instead of fp32 [n][256].
+template <bool RMS, bool SPLIT>
+static engram_status query_launch(const engram_config *cfg, const uint16_t *A, int K, const uint16_t *B, void *out,
+                                  int64_t n_query, cudaStream_t st) {
+    layer::QParams p;
+    p.out = out;
+    p.n_query = n_query;
+    p.m_tiles = (n_query + layer::BM - 1) / layer::BM;
+    p.d = K;
+    p.eps = cfg->rms_eps;
+    CUtensorMap amap, bmap;
+    if (!bf16_map_2d(&amap, A, (uint64_t)K, (uint64_t)n_query, layer::BK, layer::BM))
+        return cuda_fail(cudaErrorInvalidValue, "query A map");
+    if (!bf16_map_2d(&bmap, B, kLayerWidth, (uint64_t)K, 64, layer::BK))
+        return cuda_fail(cudaErrorInvalidValue, "query B map");
+    auto kern = layer::query_kernel<RMS, SPLIT>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, layer::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(query smem)");
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    const unsigned grid = (unsigned)std::min<int64_t>(p.m_tiles, num_sms());
+    kern<<<grid, layer::NUM_THREADS, layer::SMEM_BYTES, st>>>(amap, bmap, p);
+    return launch_status();
 }
 
 engram_status check_fuse_args(const engram_config *cfg, const void *W, const void *g, const void *h) {
@@ -1086,6 +1267,74 @@ extern "C" engram_status engram_host_free(void *ptr) {
     const cudaError_t e = cudaHostUnregister(ptr);
     munmap(m.first, m.second);
     return e == cudaSuccess ? ENGRAM_OK : cuda_fail(e, "cudaHostUnregister");
+}
+
+// ============================================ per-layer Engram (row gates) ==
+
+extern "C" engram_status engram_layer_keys(const engram_config *cfg, const uint16_t *W_k, uint16_t *W_kk,
+                                           void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || !W_k || !W_kk) return ENGRAM_EINVAL;
+    if (!aligned(W_k, 16) || !aligned(W_kk, 16)) return ENGRAM_EINVAL;
+    layer::wkk_kernel<<<2 * kLayerWidth, kLayerWidth, 0, (cudaStream_t)stream>>>(W_k, W_kk);
+    return launch_status();
+}
+
+// workspace: q pair bf16 [n][512] | u fp32 [n][256] | X bf16 [n][256]
+static size_t layer_off_u(int64_t n) { return round_up((size_t)n * 2 * kLayerWidth * 2, 256); }
+static size_t layer_off_x(int64_t n) { return layer_off_u(n) + round_up((size_t)n * kLayerWidth * 4, 256); }
+
+extern "C" size_t engram_layer_workspace_bytes(const engram_config *cfg, int64_t n_query) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0) return 0;
+    return layer_off_x(n_query) + round_up((size_t)n_query * kLayerWidth * 2, 256);
+}
+
+extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t module, const int32_t *tokens,
+                                              const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                              int64_t n_query, const uint8_t *tables, const float *scales,
+                                              const uint16_t *W_q, const uint16_t *W_kk, const uint16_t *W_m,
+                                              uint16_t *h, void *workspace, size_t workspace_bytes, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || module < 0 || module > 1 || n_query < 0 || n_seqs < 0 || last_n < 0)
+        return ENGRAM_EINVAL;
+    if (mx(cfg)) return ENGRAM_EUNSUPPORTED;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales_ok(cfg, scales) || !W_q || !W_kk || !W_m ||
+        !h || !workspace)
+        return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    const int d = cfg->d_model;
+    if (d < fuse::BN || d % fuse::BN != 0 || d > 16 * fuse::BN * fuse::MAX_GROUPS) return ENGRAM_EINVAL;
+    if (!aligned(tables, 16) || !aligned(W_q, 16) || !aligned(W_kk, 16) || !aligned(W_m, 16) || !aligned(h, 16) ||
+        !aligned(workspace, 256) || !aligned(tokens, 4) || !aligned(seq_offsets, 8))
+        return ENGRAM_EINVAL;
+    if (!(cfg->rms_eps >= 0.0f) || n_query > (INT64_C(1) << 40)) return ENGRAM_EINVAL;
+    if (workspace_bytes < engram_layer_workspace_bytes(cfg, n_query)) return ENGRAM_ENOMEM;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint16_t *qpair = reinterpret_cast<uint16_t *>(ws);
+    float *u = reinterpret_cast<float *>(ws + layer_off_u(n_query));
+    uint16_t *X = reinterpret_cast<uint16_t *>(ws + layer_off_x(n_query));
+    // q = rinv(h) h W_q as a bf16 pair, then u = [q_hi | q_lo] [W_k^T ; W_k^T]
+    engram_status s = query_launch<true, true>(cfg, h, d, W_q, qpair, n_query, st);
+    if (s != ENGRAM_OK) return s;
+    s = query_launch<false, false>(cfg, qpair, 2 * kLayerWidth, W_kk, u, n_query, st);
+    if (s != ENGRAM_OK) return s;
+    GatedParams P;
+    memset(&P, 0, sizeof(P));
+    P.rows = tables;
+    P.scales = scales_arg(cfg, scales);
+    P.row_stride = row_stride(cfg);
+    P.q = u;
+    P.X = X;
+    P.n_query = n_query;
+    P.R = cfg->rows;
+    P.module = module;
+    P.eps = cfg->rms_eps;
+    fill_hash_params(P.hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
+    const unsigned blocks = (unsigned)((n_query * 32 + 255) / 256);
+    gather_gated_kernel<<<blocks, 256, 0, st>>>(P);
+    s = launch_status();
+    if (s != ENGRAM_OK) return s;
+    return layer_projection_launch(cfg, X, W_m, h, n_query, st);
 }
 
 // ================================================== pipelined host path ====

@@ -82,7 +82,11 @@ static_assert(RING_STAGE_BYTES % 1024 == 0 && X_KBLOCK_BYTES % 1024 == 0, "swizz
 // warps 2, 3 -> gate warps 0, 1; warps 12..15 -> gate warps 2..5
 __device__ __forceinline__ int gate_warp_index(int warp) { return warp < 4 ? warp - 2 : warp - 10; }
 
-template <int CPG>
+// KB: 64-wide K-blocks of X (8: the concatenated [T,512] X; 4: one Engram
+// layer's [T,256] X).  GATED: the rmsnorm-sigmoid token gate of the concatenated
+// form; without it h = bf16(h + y) (the per-layer form gates rows before the
+// projection) and the gate warps stay idle.
+template <int CPG, int KB = KSTAGES, bool GATED = true>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fuse2_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
                  const __grid_constant__ Params p) {
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued_parity[NSTAGE] = {};
             for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl) {
                 for (int c = c0; c < c0 + CPG && !*abort; ++c) {
-                    for (int ks = 0; ks < KSTAGES; ++ks) {
+                    for (int ks = 0; ks < KB; ++ks) {
                         if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort)) break;
                         mbar_arrive_expect_tx(&sh->full[stage], RING_STAGE_BYTES);
                         uint8_t *dst = ring + stage * RING_STAGE_BYTES;
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!mbar_wait(&sh->acc_empty[buf], (use & 1u) ^ 1u, abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int ks = 0; ks < KSTAGES; ++ks) {
+                    for (int ks = 0; ks < KB; ++ks) {
                         if (!mbar_wait(&sh->full[stage], phase, abort)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t st_addr = ring_addr + stage * RING_STAGE_BYTES;
@@ -216,21 +220,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl, ++it) {
             const int64_t m0 = mt * BM;
             const uint32_t pb = it & 1u;
-            if (!mbar_wait_cluster(&sh->part_full[pb], (it >> 1) & 1u, abort)) break;
-            float ssum = 0.f, dsum = 0.f;
-            const uint32_t my_part = smem_u32(&sh->part[pb][row]);
-            for (int r = 0; r < p.groups; ++r) {  // same order in every CTA
-                const float2 v = ld_shared_cluster_f2(mapa_shared(my_part, (uint32_t)r));
-                ssum += v.x;
-                dsum += v.y;
-            }
-            const float rinv = rsqrtf(ssum / (float)p.d + p.eps);
-            const float gate = 1.f / (1.f + __expf(-(rinv * dsum * p.inv_sqrt_d)));
-            __syncwarp();
-            if (lane == 0) {  // this warp is done with part[pb] of every CTA
-                const uint32_t bar = smem_u32(&sh->part_free[pb]);
-                for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
-                if (LEAD_CHUNK < 0 || LEAD_CHUNK >= CPG) mbar_arrive(&sh->upd_mark[pb]);
+            float gate = 1.f;
+            if constexpr (GATED) {
+                if (!mbar_wait_cluster(&sh->part_full[pb], (it >> 1) & 1u, abort)) break;
+                float ssum = 0.f, dsum = 0.f;
+                const uint32_t my_part = smem_u32(&sh->part[pb][row]);
+                for (int r = 0; r < p.groups; ++r) {  // same order in every CTA
+                    const float2 v = ld_shared_cluster_f2(mapa_shared(my_part, (uint32_t)r));
+                    ssum += v.x;
+                    dsum += v.y;
+                }
+                const float rinv = rsqrtf(ssum / (float)p.d + p.eps);
+                gate = 1.f / (1.f + __expf(-(rinv * dsum * p.inv_sqrt_d)));
+                __syncwarp();
+                if (lane == 0) {  // this warp is done with part[pb] of every CTA
+                    const uint32_t bar = smem_u32(&sh->part_free[pb]);
+                    for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+                    if (LEAD_CHUNK < 0 || LEAD_CHUNK >= CPG) mbar_arrive(&sh->upd_mark[pb]);
+                }
             }
 
             // h = bf16(h + gate * y) on this warp's 32 rows and 128 columns of
@@ -286,7 +293,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int k = 0; k < 4; ++k) {
                             const float y0 = __uint_as_float(y[8 * k4 + 2 * k]);
                             const float y1 = __uint_as_float(y[8 * k4 + 2 * k + 1]);
-                            w[k] = pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])));
+                            w[k] = GATED ? pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])))
+                                         : pack_bf16x2(bf16_lo(w[k]) + y0, bf16_hi(w[k]) + y1);
                         }
                         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
                     }
@@ -304,14 +312,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_before();
                     if (lane == 0) {
                         mbar_arrive(&sh->acc_empty[buf]);
-                        if (c == LEAD_CHUNK) mbar_arrive(&sh->upd_mark[pb]);
+                        if (GATED && c == LEAD_CHUNK) mbar_arrive(&sh->upd_mark[pb]);
                     }
                 }
             }
             acc_it += CPG;
             if (!ok) break;
         }
-    } else {
+    } else if (GATED) {
         // --------------------------------------------------- gate warps -----
         // Rows in batches of RB (16 16-byte loads per lane in flight), batch b
         // on gate warp b mod 6.  Lanes stride over each row's 16-byte pieces;

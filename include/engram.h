@@ -281,6 +281,39 @@ engram_status engram_forward_host(const engram_config *cfg, const int32_t *token
  * set the sticky error word.
  */
 /*
+ * The per-layer form of the Engram read (rohitghumare.com
+ * "guides/deepseek-v4-1-flash": section "The architecture", layers 1 and 14
+ * each add looked-up rows into the residual stream through a learned gate;
+ * section "Engram: the table that is never multiplied", 24 rows per Engram
+ * layer and a gate that compares each retrieved row with the hidden state).
+ * Layer m in {0, 1} uses module m's 24 tables (24m .. 24m+23) and, per the
+ * reading the pages leave open,
+ *   g_j = sigmoid(<rmsnorm(h) W_q, rmsnorm(r_j) W_k> / 16)   per row r_j,
+ *   h   = bf16(h + bf16(sum_j g_j r_j) W_m),
+ * rmsnorm without a weight (eps = cfg->rms_eps), r_j = scale * e4m3 value.
+ *
+ * engram_layer_keys: W_kk [512][256] = [W_k^T ; W_k^T] (bf16 copies) from
+ *   W_k [256][256] (bf16, device); once per set of weights.
+ * engram_layer_forward: one layer, in place on h [n_query][d] bf16, from the
+ *   HBM tables (ENGRAM_ROWS_SEPARATE or ENGRAM_ROWS_RECORD; MX rows are
+ *   ENGRAM_EUNSUPPORTED), W_q [d][256], W_kk and W_m [256][d] (bf16, device).
+ *   Kernels: q = rinv(h) h W_q (tcgen05, written as bf16 q_hi | q_lo), u =
+ *   [q_hi | q_lo] W_kk = q W_k^T (tcgen05), the gated gather (hash, gather,
+ *   score_j = <u, rmsnorm(r_j)> / 16, X = bf16 [n][256]), the projection.
+ *   workspace >= engram_layer_workspace_bytes: q pair bf16 [n][512], u fp32
+ *   [n][256], X bf16 [n][256], each 256-byte aligned.  Argument errors return
+ *   synchronously; device range errors set the sticky error word.  d must be
+ *   a multiple of 256.
+ */
+engram_status engram_layer_keys(const engram_config *cfg, const uint16_t *W_k, uint16_t *W_kk, void *stream);
+size_t engram_layer_workspace_bytes(const engram_config *cfg, int64_t n_query);
+engram_status engram_layer_forward(const engram_config *cfg, int32_t module, const int32_t *tokens,
+                                   const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n, int64_t n_query,
+                                   const uint8_t *tables, const float *scales, const uint16_t *W_q,
+                                   const uint16_t *W_kk, const uint16_t *W_m, uint16_t *h, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * Pinned host memory for host tables (engram_stage, engram_forward_host,
  * engram_forward_host_pipelined), mapped on transparent huge pages where the
  * operating system offers them and registered with the CUDA driver, so the

@@ -18,6 +18,9 @@ STREAM_H = 0x300  # word = t*d + c
 STREAM_W = 0x301  # word = k*d + c
 STREAM_G = 0x302  # word = c
 STREAM_MX = 0x400  # + table j: eight u32 per row (one per E8M0 block scale), word = row*8 + b
+STREAM_WQ = 0x500  # + layer m: per-row gate query weights W_q [d][256], word = i*256 + c
+STREAM_WK = 0x510  # + layer m: per-row gate key weights W_k [256][256], word = i*256 + c
+STREAM_WM = 0x520  # + layer m: layer projection W_m [256][d], word = c*d + n
 
 N_TABLES = 48
 ROW_BYTES = 256

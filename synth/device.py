@@ -13,7 +13,7 @@ import subprocess
 import numpy as np
 import torch
 
-from .configs import N_TABLES, ROW_BYTES, STREAM_G, STREAM_H, STREAM_W
+from .configs import N_TABLES, ROW_BYTES, STREAM_G, STREAM_H, STREAM_W, STREAM_WK, STREAM_WM, STREAM_WQ
 from .host import W_SIGMA, bf16_table, e4m3_table
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -126,6 +126,14 @@ def fill_h(dst, seed):
 
 def fill_w_out(dst, seed):
     fill_bf16(dst, seed, STREAM_W, W_SIGMA)
+
+
+def fill_layer_weights(wq, wk, wm, seed, m):
+    """Device twin of host.layer_weights for Engram layer m."""
+    d = wq.shape[0]
+    fill_bf16(wq, seed, STREAM_WQ + m, 1.0 / np.sqrt(d))
+    fill_bf16(wk, seed, STREAM_WK + m, 1.0 / 16.0)
+    fill_bf16(wm, seed, STREAM_WM + m, 1.0 / 16.0)
 
 
 def fill_g(dst, seed):

@@ -18,6 +18,9 @@ from .configs import (
     STREAM_SCALE,
     STREAM_TABLE,
     STREAM_W,
+    STREAM_WK,
+    STREAM_WM,
+    STREAM_WQ,
 )
 from .philox import philox4x64, philox_u32
 from .sampler import bf16_normal_table, e4m3_normal_table, sample_codes, scale_from_u32
@@ -91,6 +94,15 @@ def h_rows(seed, d, t_idx):
 def w_out(seed, d):
     """W_out bf16 bits [512, d], N(0, 1/512)."""
     return bf16_words(seed, STREAM_W, W_SIGMA, 0, 512 * d).reshape(512, d)
+
+
+def layer_weights(seed, d, m):
+    """Per-layer gate and projection weights (bf16 bits) of Engram layer m:
+    W_q [d,256] ~ N(0,1/d), W_k [256,256] ~ N(0,1/256), W_m [256,d] ~ N(0,1/256)."""
+    wq = bf16_words(seed, STREAM_WQ + m, 1.0 / np.sqrt(d), 0, d * 256).reshape(d, 256)
+    wk = bf16_words(seed, STREAM_WK + m, 1.0 / 16.0, 0, 256 * 256).reshape(256, 256)
+    wm = bf16_words(seed, STREAM_WM + m, 1.0 / 16.0, 0, 256 * d).reshape(256, d)
+    return wq, wk, wm
 
 
 def g_vec(seed, d):
