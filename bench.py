@@ -324,6 +324,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     host = cfg.host_tables
+    layers = args.variant == "layers"
+    if layers:  # the per-layer form: layer 0 (module 0) then layer 1 (module 1), per-row gates
+        if host or args.layout == "mx":
+            raise SystemExit("--variant layers runs on HBM tables with fp32 row scales")
+        lw = []
+        for m in (0, 1):
+            wq = torch.empty((cfg.d, 256), dtype=torch.bfloat16, device=dev)
+            wk = torch.empty((256, 256), dtype=torch.bfloat16, device=dev)
+            wm = torch.empty((256, cfg.d), dtype=torch.bfloat16, device=dev)
+            sd.fill_layer_weights(wq, wk, wm, base.seed, m)
+            lw.append((wq, eg.engram_layer_keys(c, wk), wm))
+        lws = torch.empty(eg.engram_layer_workspace_bytes(c, nq), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
     if host:
         cap = nq * 48
         fws = torch.empty(eg.engram_forward_host_workspace_bytes(c, nq, cap), dtype=torch.uint8, device=dev)
@@ -341,6 +354,15 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None:
                 ev[1].record(stream)
             return 9  # hash, 5 dedup kernels, stage, staged gather, fuse
+        if layers:
+            for m in (0, 1):
+                if ev is not None:
+                    ev[m].record(stream)
+                eg.engram_layer_forward(c, m, tokens, seq_offsets, tables, scales, lw[m][0], lw[m][1], lw[m][2], h,
+                                        last_n=cfg.last_n, n_query=nq, workspace=lws)
+            if ev is not None:
+                ev[2].record(stream)
+            return 8  # per layer: query, key-side query, gated gather, projection
         if ev is not None:
             ev[0].record(stream)
         eg.engram_gather_x(c, tokens, seq_offsets, tables, scales, last_n=cfg.last_n, n_query=nq, X=X)
@@ -388,18 +410,25 @@ def run_ours(args, rank, world, local_rank):
                f"no flush: table rows random over {48 * cfg.R * rb / 1e9:.1f} GB, but h, X and W_out "
                f"({resident / 1e6:.1f} MB) stay in L2 between steps")
     cuda_graph = None
-    if not host and nq <= 4096:  # decode-sized batches: launch latency matters
+    if not host and not layers and nq <= 4096:  # decode-sized batches: launch latency matters
         cuda_graph = time_forward_graph(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
                                         max(K, 200))
 
     peaks = measured_peaks()
     per_kernel_ms = {}
-    if not host:
+    if layers:
+        per_kernel_ms = {
+            "layer0": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
+            "layer1": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
+        }
+    elif not host:
         per_kernel_ms = {
             "gather": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
             "fuse": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
         }
-    kb = kernel_bytes_per_token(cfg.d, args.layout)
+    # algorithmic bytes per token; a layer moves its 24 rows + scales and h once each way
+    kb = ({"layer0": 4 + 24 * 260 + 4 * cfg.d, "layer1": 4 + 24 * 260 + 4 * cfg.d} if layers
+          else kernel_bytes_per_token(cfg.d, args.layout))
     kernels = {}
     for name, kms in per_kernel_ms.items():
         gbs = kb[name] * nq / (kms * 1e-3) / 1e9
@@ -408,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
     if per_kernel_ms:
         dom = max(per_kernel_ms, key=per_kernel_ms.get)
         ach = kb[dom] * nq / (per_kernel_ms[dom] * 1e-3) / 1e9
-        tr = None if (args.rows or args.tokens) else ncu_traffic(dom, args.workload, nq, args.layout)
+        tr = None if (args.rows or args.tokens or layers) else ncu_traffic(dom, args.workload, nq, args.layout)
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": tr,
                     "algorithmic_bytes_per_launch": kb[dom] * nq,
@@ -417,7 +446,8 @@ def run_ours(args, rank, world, local_rank):
     if host:
         roofline = host_link_roofline(eg, c, cfg, tokens, seq_offsets, tables, scales, nq, dev)
 
-    step_gbs = nominal_bytes_per_token(cfg.d) * nq / (ms_max * 1e-3 / K) / 1e9
+    nominal = 2 * (24 * 256 + 4 * cfg.d) if layers else nominal_bytes_per_token(cfg.d)
+    step_gbs = nominal * nq / (ms_max * 1e-3 / K) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -433,10 +463,15 @@ def run_ours(args, rank, world, local_rank):
                                   "separate": "256-byte rows + separate fp32 scale array"}[args.layout],
                    "token_ids": ("uniform" if cfg.zipf_s == 0 else f"Zipf({cfg.zipf_s})"),
                    "l2": l2_note, "parallelism": f"dp{world} (replicated tables)"},
-        "step_roofline": {"nominal_bytes_per_token": nominal_bytes_per_token(cfg.d), "achieved_GBps": round(step_gbs, 1),
+        "step_roofline": {"nominal_bytes_per_token": nominal, "achieved_GBps": round(step_gbs, 1),
                           "peak_GBps": peaks["hbm_gbs"], "frac": round(step_gbs / peaks["hbm_gbs"], 4)},
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
     }
+    if layers:
+        out["config"]["variant"] = ("per-layer: layer 0 (module 0) then layer 1 (module 1), 24 rows each, "
+                                    "per-row gates sigmoid(<rmsnorm(h) W_q, rmsnorm(r) W_k> / 16), W_m 256 x d")
+        out["dtype"] = ("e4m3->f32 gather, bf16 x bf16 -> f32 query / key / projection (q as two bf16 halves), "
+                        "bf16 residual")
     if cuda_graph is not None:
         out["cuda_graph"] = cuda_graph
     if host:
@@ -446,9 +481,9 @@ def run_ours(args, rank, world, local_rank):
         out["pipelined"] = [time_host_pipelined(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
                                                 ch, max(3, min(K, 20)))
                             for ch in args.host_chunks if 0 < ch < nq]
-    if not args.no_e2e:
+    if not args.no_e2e and not layers:
         out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not layers:
         out["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     return out
 
@@ -667,6 +702,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large", choices=["tiny", "decode", "prefill", "large", "host"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="concat", choices=["concat", "layers"],
+                    help="concat: one [T,512] projection with a token gate (the headline path); layers: two "
+                         "Engram layers with per-row gates")
     ap.add_argument("--layout", default="separate", choices=["record", "separate", "mx"],
                     help="table rows that carry their fp32 scale (record), MXFP8-style rows with eight E8M0 "
                          "block scales (mx), or a separate scale array")
