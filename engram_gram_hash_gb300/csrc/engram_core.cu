@@ -316,46 +316,54 @@ __global__ void __launch_bounds__(256, 2) gather_gated_kernel(const __grid_const
         v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);
         if (__shfl_sync(0xffffffffu, ok, src)) live |= 1u << i;
     }
-    float acc[16];
+    // Per row, on the raw e4m3 values c (the row's scale s factors out):
+    // sum(r^2) = s^2 sum(c^2), <u, r> = s <u, c>, and the gated sum takes
+    // (g s) c.  Pairs of columns go through packed fp32 FMAs.
+    float2 acc[8];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    for (int k = 0; k < 8; ++k) acc[k] = make_float2(0.f, 0.f);
+    float2 u2[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) u2[k] = make_float2(qv[2 * k], qv[2 * k + 1]);
 #pragma unroll
     for (int i = 0; i < 12; ++i) {
-        float f[16];
+        float2 c[8];
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            const float2 a = e4m3x2_to_float2((uint16_t)(w[q4] & 0xFFFFu));
-            const float2 b = e4m3x2_to_float2((uint16_t)(w[q4] >> 16));
-            f[4 * q4 + 0] = s[i] * a.x;
-            f[4 * q4 + 1] = s[i] * a.y;
-            f[4 * q4 + 2] = s[i] * b.x;
-            f[4 * q4 + 3] = s[i] * b.y;
+            c[2 * q4] = e4m3x2_to_float2((uint16_t)(w[q4] & 0xFFFFu));
+            c[2 * q4 + 1] = e4m3x2_to_float2((uint16_t)(w[q4] >> 16));
         }
-        float ss = 0.f, dd = 0.f;
+        float2 ss2 = make_float2(0.f, 0.f), dd2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            ss = fmaf(f[k], f[k], ss);
-            dd = fmaf(f[k], qv[k], dd);
+        for (int k = 0; k < 8; ++k) {
+            ss2 = fma2(c[k], c[k], ss2);
+            dd2 = fma2(c[k], u2[k], dd2);
         }
+        float ss = ss2.x + ss2.y, dd = dd2.x + dd2.y;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) {  // over the 16 lanes of this half-warp
             ss += __shfl_xor_sync(0xffffffffu, ss, o);
             dd += __shfl_xor_sync(0xffffffffu, dd, o);
         }
-        const float score = rsqrtf(ss * (1.f / 256.f) + P.eps) * dd * (1.f / 16.f);
-        const float g = (live >> i) & 1u ? 1.f / (1.f + __expf(-score)) : 0.f;
+        const float sc = s[i];
+        const float score = rsqrtf(sc * sc * ss * (1.f / 256.f) + P.eps) * sc * dd * (1.f / 16.f);
+        const float gs = (live >> i) & 1u ? sc / (1.f + __expf(-score)) : 0.f;
+        const float2 g2 = make_float2(gs, gs);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = fmaf(g, f[k], acc[k]);
+        for (int k = 0; k < 8; ++k) acc[k] = fma2(g2, c[k], acc[k]);
     }
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
+    for (int k = 0; k < 8; ++k) {
+        acc[k].x += __shfl_xor_sync(0xffffffffu, acc[k].x, 16);
+        acc[k].y += __shfl_xor_sync(0xffffffffu, acc[k].y, 16);
+    }
     if (half == 0) {
         uint4 *dst = reinterpret_cast<uint4 *>(P.X + t * kLayerWidth + c16 * 16);
-        dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                            pack_bf16x2(acc[6], acc[7]));
-        dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                            pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+        dst[0] = make_uint4(pack_bf16x2(acc[0].x, acc[0].y), pack_bf16x2(acc[1].x, acc[1].y),
+                            pack_bf16x2(acc[2].x, acc[2].y), pack_bf16x2(acc[3].x, acc[3].y));
+        dst[1] = make_uint4(pack_bf16x2(acc[4].x, acc[4].y), pack_bf16x2(acc[5].x, acc[5].y),
+                            pack_bf16x2(acc[6].x, acc[6].y), pack_bf16x2(acc[7].x, acc[7].y));
     }
 }
 
