@@ -852,26 +852,30 @@ static auto fuse_kernel_for() {
 }
 
 template <int KIND, int CPG>
-static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
-                                   cudaStream_t st) {
+static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hmap,
+                                   const fuse::Params &p, cudaStream_t st) {
     constexpr bool k2 = KIND == FUSE_BF16_X_GATE_WARPS || KIND == FUSE_LAYER;
     constexpr int kThreads = k2 ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
     constexpr int kSmem = k2 ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
     static bool attr_done[64] = {};
     static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
-    return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
-                             max_clusters, st, wmap, xmap, p);
+    if constexpr (k2)
+        return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
+                                 max_clusters, st, wmap, xmap, hmap, p);
+    else
+        return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
+                                 max_clusters, st, wmap, xmap, p);
 }
 
 template <int KIND>
-static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &xmap, const fuse::Params &p,
-                                   cudaStream_t st) {
+static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hmap,
+                                   const fuse::Params &p, cudaStream_t st) {
     switch (p.cpg) {
-        case 1: return fuse_launch_t<KIND, 1>(wmap, xmap, p, st);
-        case 2: return fuse_launch_t<KIND, 2>(wmap, xmap, p, st);
-        case 4: return fuse_launch_t<KIND, 4>(wmap, xmap, p, st);
-        case 8: return fuse_launch_t<KIND, 8>(wmap, xmap, p, st);
-        case 16: return fuse_launch_t<KIND, 16>(wmap, xmap, p, st);
+        case 1: return fuse_launch_t<KIND, 1>(wmap, xmap, hmap, p, st);
+        case 2: return fuse_launch_t<KIND, 2>(wmap, xmap, hmap, p, st);
+        case 4: return fuse_launch_t<KIND, 4>(wmap, xmap, hmap, p, st);
+        case 8: return fuse_launch_t<KIND, 8>(wmap, xmap, hmap, p, st);
+        case 16: return fuse_launch_t<KIND, 16>(wmap, xmap, hmap, p, st);
     }
     return ENGRAM_EINVAL;
 }
@@ -927,16 +931,21 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     if (x_bf16) {
         if (!bf16_map_2d(&xmap, x_bf16, kMem, (uint64_t)n_query, fuse::BK, fuse::BM))
             return cuda_fail(cudaErrorInvalidValue, "X tensor map");
-        if (cpg3 != 0) {
+        if (cpg3 == 0) {  // h pieces of 64 columns x 32 tokens for the update warps' TMA loads and stores
+            CUtensorMap hp;
+            if (!bf16_map_2d(&hp, h, (uint64_t)d, (uint64_t)n_query, 64, 32))
+                return cuda_fail(cudaErrorInvalidValue, "h piece map");
+            return fuse_dispatch<FUSE_BF16_X_GATE_WARPS>(wmap, xmap, hp, p, st);
+        }
+        {
             CUtensorMap hl, hs;  // h slice boxes: 64 columns x 128 tokens (loads) / x 32 tokens (stores)
             if (!bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, 64, fuse::BM) ||
                 !bf16_map_2d(&hs, h, (uint64_t)d, (uint64_t)n_query, 64, 32))
                 return cuda_fail(cudaErrorInvalidValue, "h tensor map");
             return cpg3 == 1 ? fuse3_launch_t<1>(wmap, xmap, hl, hs, p, st) : fuse3_launch_t<2>(wmap, xmap, hl, hs, p, st);
         }
-        return fuse_dispatch<FUSE_BF16_X_GATE_WARPS>(wmap, xmap, p, st);
     }
-    return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, p, st);
+    return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, xmap, p, st);
 }
 
 // One Engram layer's projection: h = bf16(h + X W_m), X [n][256] bf16,
@@ -960,7 +969,9 @@ static engram_status layer_projection_launch(const engram_config *cfg, const uin
     if (!bf16_map_2d(&wmap, W, (uint64_t)d, kLayerWidth, 64, fuse::BK)) return cuda_fail(cudaErrorInvalidValue, "W_m map");
     if (!bf16_map_2d(&xmap, X, kLayerWidth, (uint64_t)n_query, fuse::BK, fuse::BM))
         return cuda_fail(cudaErrorInvalidValue, "layer X map");
-    return fuse_dispatch<FUSE_LAYER>(wmap, xmap, p, st);
+    CUtensorMap hp;
+    if (!bf16_map_2d(&hp, h, (uint64_t)d, (uint64_t)n_query, 64, 32)) return cuda_fail(cudaErrorInvalidValue, "h piece map");
+    return fuse_dispatch<FUSE_LAYER>(wmap, xmap, hp, p, st);
 }
 
 // out = s * (A @ B) on tcgen05 (layer::query_kernel): A bf16 [n][K], B bf16

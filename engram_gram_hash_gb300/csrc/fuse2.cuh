@@ -50,7 +50,12 @@ using fuse::X_KBLOCK_BYTES;
 
 constexpr int W_BOX_BYTES = BK * 64 * 2;                      // 8 KB: 64 K-rows x 64 N
 constexpr int RING_STAGE_BYTES = X_KBLOCK_BYTES + W_BOX_BYTES * (BN / 64);  // 16 KB X + 32 KB W
-constexpr int NSTAGE = 4;
+// The update warps move h pieces (32 tokens x 64 columns) with TMA loads and
+// stores through two staging buffers each (kTmaUpdate), or through registers
+// and one buffer; the TMA form leaves room for 3 ring stages instead of 4.
+constexpr bool kTmaUpdate = true;
+constexpr int NSTAGE = kTmaUpdate ? 3 : 4;
+constexpr int STG_BUFS = kTmaUpdate ? 2 : 1;
 
 constexpr int UPDATE_WARPS = 8;  // warps 4..11
 // The gate warps start reading tile i+1 once the update warps have finished
@@ -69,13 +74,14 @@ struct Shared {
     uint64_t part_full[2];
     uint64_t part_free[2];
     uint64_t upd_mark[2];  // local: the update warps reached chunk LEAD_CHUNK of a tile
+    uint64_t hb_full[8][2];  // per update warp and staging buffer: a TMA-loaded h piece landed
     uint64_t done;
     uint32_t tmem_base;
     int abort;
     float2 part[2][BM];  // (sum h^2, <h,g>) over this CTA's slice, per token
 };
 
-constexpr int SMEM_BYTES = NSTAGE * RING_STAGE_BYTES + UPDATE_WARPS * STAGE_BYTES + (int)sizeof(Shared);
+constexpr int SMEM_BYTES = NSTAGE * RING_STAGE_BYTES + UPDATE_WARPS * STG_BUFS * STAGE_BYTES + (int)sizeof(Shared);
 static_assert(SMEM_BYTES <= 232448, "fuse2 kernel shared memory over the per-CTA limit");
 static_assert(RING_STAGE_BYTES % 1024 == 0 && X_KBLOCK_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
 
@@ -89,7 +95,7 @@ __device__ __forceinline__ int gate_warp_index(int warp) { return warp < 4 ? war
 template <int CPG, int KB = KSTAGES, bool GATED = true>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fuse2_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
-                 const __grid_constant__ Params p) {
+                 const __grid_constant__ CUtensorMap h_map, const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_u32(smem) & 1023u) != 0) {  // same for every CTA: all leave together
         if (threadIdx.x == 0) raise_error(ENGRAM_EUNSUPPORTED);
@@ -97,7 +103,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     uint8_t *ring = smem;
     uint8_t *stage_smem = ring + NSTAGE * RING_STAGE_BYTES;
-    Shared *sh = reinterpret_cast<Shared *>(stage_smem + UPDATE_WARPS * STAGE_BYTES);
+    Shared *sh = reinterpret_cast<Shared *>(stage_smem + UPDATE_WARPS * STG_BUFS * STAGE_BYTES);
     volatile int *abort = &sh->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -119,12 +125,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&sh->part_full[b], GATE_WARPS * p.groups);
             mbar_init(&sh->part_free[b], UPDATE_WARPS * p.groups);
             mbar_init(&sh->upd_mark[b], UPDATE_WARPS);
+            for (int w = 0; w < UPDATE_WARPS; ++w) mbar_init(&sh->hb_full[w][b], 1);
         }
         mbar_init(&sh->done, 1);
         sh->abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&w_map);
         prefetch_tensormap(&x_map);
+        if (kTmaUpdate) prefetch_tensormap(&h_map);
     }
     if (warp == 1) {
         tmem_alloc(&sh->tmem_base, TMEM_COLS);
@@ -217,6 +225,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = q * 32 + lane;  // token row within the tile owned by this thread
         uint32_t it = 0;
         uint32_t acc_it = 0;
+        uint32_t gp = 0;  // h pieces this warp has handled (staging buffer gp & 1)
+        uint32_t loaded = 0;  // h pieces this warp has requested by TMA (lane 0)
+        uint8_t *const stg0 = stage_smem + ew * STG_BUFS * STAGE_BYTES;
+        if (kTmaUpdate && lane == 0 && cl < p.m_tiles) {  // the first piece
+            mbar_arrive_expect_tx(&sh->hb_full[ew][0], STAGE_BYTES);
+            tma_load_2d(stg0, &h_map, &sh->hb_full[ew][0], (int)(col0 + ch * 128), (int)(cl * BM + q * 32));
+            loaded = 1;
+        }
         for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl, ++it) {
             const int64_t m0 = mt * BM;
             const uint32_t pb = it & 1u;
@@ -240,6 +256,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
 
+            if constexpr (kTmaUpdate) {
+                // h = bf16(h + gate * y) on this warp's 32 rows and 128 columns
+                // of each chunk, in pieces of 64 columns: each piece comes in
+                // by TMA (128-byte swizzle: 16-byte chunk c of row r at c ^ (r &
+                // 7)) into one of two staging buffers while the previous piece
+                // is updated in place and leaves by TMA store.  Rows past the
+                // last token are zero-filled on load and clipped on store.
+                bool ok = true;
+                for (int pc = 0; pc < 2 * CPG; ++pc, ++gp) {
+                    const int c = pc >> 1, sub = pc & 1;
+                    const uint32_t buf = (acc_it + c) & 1u;
+                    const uint32_t use = (acc_it + c) >> 1;
+                    const uint32_t sb = gp & 1u;
+                    if (lane == 0) {
+                        // the next piece (this tile's, or the first of the next tile)
+                        const bool last = pc + 1 == 2 * CPG;
+                        const int64_t mt_n = last ? mt + n_cl : mt;
+                        if (mt_n < p.m_tiles) {
+                            const int pn = last ? 0 : pc + 1;
+                            bulk_wait_group_read0();  // that buffer's previous store has read it
+                            mbar_arrive_expect_tx(&sh->hb_full[ew][sb ^ 1u], STAGE_BYTES);
+                            tma_load_2d(stg0 + (sb ^ 1u) * STAGE_BYTES, &h_map, &sh->hb_full[ew][sb ^ 1u],
+                                        (int)(col0 + (pn >> 1) * BN + ch * 128 + (pn & 1) * 64), (int)(mt_n * BM + q * 32));
+                            loaded = gp + 2;
+                        }
+                    }
+                    if (!mbar_wait(&sh->hb_full[ew][sb], (gp >> 1) & 1u, abort)) { ok = false; break; }
+                    if (sub == 0) {
+                        if (!mbar_wait(&sh->acc_full[buf], use & 1u, abort)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    const uint32_t stg_a = smem_u32(stg0 + sb * STAGE_BYTES);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {  // own row: 32 columns at a time
+                        uint32_t y[32];
+                        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + ch * 128 + sub * 64 + half * 32, y);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const int cch = half * 4 + k4;
+                            const uint32_t addr = stg_a + lane * 128 + ((cch ^ (lane & 7)) << 4);
+                            uint32_t w[4];
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr) : "memory");
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float y0 = __uint_as_float(y[8 * k4 + 2 * k]);
+                                const float y1 = __uint_as_float(y[8 * k4 + 2 * k + 1]);
+                                w[k] = GATED ? pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])))
+                                             : pack_bf16x2(bf16_lo(w[k]) + y0, bf16_hi(w[k]) + y1);
+                            }
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();  // this thread's writes are visible to the TMA store
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&h_map, stg0 + sb * STAGE_BYTES, (int)(col0 + c * BN + ch * 128 + sub * 64),
+                                     (int)(m0 + q * 32));
+                        bulk_commit_group();
+                    }
+                    if (sub == 1) {
+                        tc_fence_before();
+                        if (lane == 0) {
+                            mbar_arrive(&sh->acc_empty[buf]);
+                            if (GATED && c == LEAD_CHUNK) mbar_arrive(&sh->upd_mark[pb]);
+                        }
+                    }
+                }
+                acc_it += CPG;
+                if (!ok) break;
+                continue;
+            }
             // h = bf16(h + gate * y) on this warp's 32 rows and 128 columns of
             // each chunk, in pieces of 64 columns, through the staging tile
             // (16-byte chunk c of row r at chunk c ^ (r & 7)); the next piece's
@@ -318,6 +406,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             acc_it += CPG;
             if (!ok) break;
+        }
+        if (kTmaUpdate && lane == 0) {
+            bulk_wait_group0();  // stores complete before the CTA leaves
+            int no_abort = 0;    // and no requested piece is still landing (after an abort)
+            for (uint32_t k = gp; k < loaded; ++k)
+                mbar_wait(&sh->hb_full[ew][k & 1u], (k >> 1) & 1u, &no_abort, 200000000ull);
         }
     } else if (GATED) {
         // --------------------------------------------------- gate warps -----
