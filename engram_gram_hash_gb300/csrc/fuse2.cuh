@@ -1,22 +1,22 @@
 // The gated projection for a bf16 X (TMA) with the gate on its own warps.
 //
-// Same tile, cluster and tcgen05 accumulators as fuse.cuh, with two changes.
+// Same tile, cluster and tcgen05 accumulators as fuse.cuh, with three changes.
 // X is not held for the whole tile: every ring stage carries the X K-block
 // (128 tokens x 64, 16 KB) beside the W block (64 x 256, 32 KB) it multiplies,
-// so the 192 KB that held X plus a 2-stage W ring become a 4-stage ring of
-// 48 KB stages.  The MMAs are fed by how many bytes are in flight per SM; this
-// triples them, for a third more traffic from L2 (X is read once per
-// 256-column chunk instead of once per tile).  And the epilogue is split in two
-// warp roles that run concurrently:
+// 3 stages of 48 KB; X is read from L2 once per 256-column chunk.  The
+// epilogue is split in two warp roles that run concurrently:
 //   - six gate warps reduce sum(h^2) and <h,g> over this CTA's d slice for
 //     the tokens of the NEXT tile while the current one is being updated, and
-//     publish the partial sums to the cluster (double-buffered);
+//     publish the partial sums to the cluster (double-buffered).  They start
+//     a tile once the update warps finish the previous tile's first chunk and
+//     load with an L2 evict-last hint, so the update warps find those lines
+//     in L2;
 //   - eight update warps (two per TMEM lane quadrant) combine the cluster's
-//     partial sums into each token's gate and apply h = bf16(h + gate * y)
-//     through a per-warp swizzled staging tile, as in fuse.cuh.
-// Sixteen warps (four per scheduler, 128 registers each) instead of ten: the
-// epilogue's memory and shared-memory round trips are hidden by more warps,
-// and the gate reduction no longer sits on the update warps' path.
+//     partial sums into each token's gate and apply h = bf16(h + gate * y) to
+//     32 x 64 pieces of h that come in and go out by TMA through two 128-byte
+//     swizzled staging buffers per warp, one piece landing while the other is
+//     updated.
+// Sixteen warps, four per scheduler, 128 registers each.
 //
 // Partial sums per token are reduced in the same order as in fuse.cuh (lanes
 // over 16-byte pieces, a butterfly over the warp, then the G CTAs in rank
@@ -51,18 +51,17 @@ using fuse::X_KBLOCK_BYTES;
 constexpr int W_BOX_BYTES = BK * 64 * 2;                      // 8 KB: 64 K-rows x 64 N
 constexpr int RING_STAGE_BYTES = X_KBLOCK_BYTES + W_BOX_BYTES * (BN / 64);  // 16 KB X + 32 KB W
 // The update warps move h pieces (32 tokens x 64 columns) with TMA loads and
-// stores through two staging buffers each (kTmaUpdate), or through registers
-// and one buffer; the TMA form leaves room for 3 ring stages instead of 4.
-constexpr bool kTmaUpdate = true;
-constexpr int NSTAGE = kTmaUpdate ? 3 : 4;
-constexpr int STG_BUFS = kTmaUpdate ? 2 : 1;
+// stores through two staging buffers each.
+constexpr int STG_BUFS = 2;
 
-constexpr int UPDATE_WARPS = 8;  // warps 4..11
+constexpr int UPDATE_WARPS = 8;  // warps 4..11: two per TMEM lane quadrant (4 measured slower)
 // The gate warps start reading tile i+1 once the update warps have finished
 // chunk LEAD_CHUNK of tile i (-1: as soon as they start tile i).  A shorter
 // lead keeps the gate warps' h reads in L2 until the update warps re-read them.
 constexpr int LEAD_CHUNK = 0;
-constexpr int GATE_WARPS = 6;    // warps 2, 3, 12..15
+constexpr int GATE_WARPS = 14 - UPDATE_WARPS;  // warps 2, 3 and 4 + UPDATE_WARPS .. 15
+constexpr int PIECES = 4 * 4 / UPDATE_WARPS;    // 64-column pieces of a chunk per update warp
+constexpr int NSTAGE = UPDATE_WARPS == 4 ? 4 : 3;  // ring stages that fit beside the staging buffers
 constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 
@@ -86,7 +85,7 @@ static_assert(SMEM_BYTES <= 232448, "fuse2 kernel shared memory over the per-CTA
 static_assert(RING_STAGE_BYTES % 1024 == 0 && X_KBLOCK_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
 
 // warps 2, 3 -> gate warps 0, 1; warps 12..15 -> gate warps 2..5
-__device__ __forceinline__ int gate_warp_index(int warp) { return warp < 4 ? warp - 2 : warp - 10; }
+__device__ __forceinline__ int gate_warp_index(int warp) { return warp < 4 ? warp - 2 : warp - 2 - UPDATE_WARPS; }
 
 // KB: 64-wide K-blocks of X (8: the concatenated [T,512] X; 4: one Engram
 // layer's [T,256] X).  GATED: the rmsnorm-sigmoid token gate of the concatenated
@@ -132,7 +131,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_mbar_init();
         prefetch_tensormap(&w_map);
         prefetch_tensormap(&x_map);
-        if (kTmaUpdate) prefetch_tensormap(&h_map);
+        prefetch_tensormap(&h_map);
     }
     if (warp == 1) {
         tmem_alloc(&sh->tmem_base, TMEM_COLS);
@@ -221,16 +220,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------- update warps -----
         const int ew = warp - 4;        // 0..7
         const int q = warp & 3;         // TMEM lane quadrant of this warp
-        const int ch = ew >> 2;         // which 128-column half of each chunk
+        const int ch = ew >> 2;         // which group of PIECES 64-column pieces of each chunk
         const int row = q * 32 + lane;  // token row within the tile owned by this thread
         uint32_t it = 0;
         uint32_t acc_it = 0;
         uint32_t gp = 0;  // h pieces this warp has handled (staging buffer gp & 1)
         uint32_t loaded = 0;  // h pieces this warp has requested by TMA (lane 0)
         uint8_t *const stg0 = stage_smem + ew * STG_BUFS * STAGE_BYTES;
-        if (kTmaUpdate && lane == 0 && cl < p.m_tiles) {  // the first piece
+        // column offset of this warp's piece k of a chunk
+        auto piece_col = [&](int k) -> int { return (ch * PIECES + k) * 64; };
+        if (lane == 0 && cl < p.m_tiles) {  // the first piece
             mbar_arrive_expect_tx(&sh->hb_full[ew][0], STAGE_BYTES);
-            tma_load_2d(stg0, &h_map, &sh->hb_full[ew][0], (int)(col0 + ch * 128), (int)(cl * BM + q * 32));
+            tma_load_2d(stg0, &h_map, &sh->hb_full[ew][0], (int)(col0 + piece_col(0)), (int)(cl * BM + q * 32));
             loaded = 1;
         }
         for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl, ++it) {
@@ -256,29 +257,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
 
-            if constexpr (kTmaUpdate) {
-                // h = bf16(h + gate * y) on this warp's 32 rows and 128 columns
+            {
+                // h = bf16(h + gate * y) on this warp's 32 rows and its columns
                 // of each chunk, in pieces of 64 columns: each piece comes in
                 // by TMA (128-byte swizzle: 16-byte chunk c of row r at c ^ (r &
                 // 7)) into one of two staging buffers while the previous piece
                 // is updated in place and leaves by TMA store.  Rows past the
                 // last token are zero-filled on load and clipped on store.
                 bool ok = true;
-                for (int pc = 0; pc < 2 * CPG; ++pc, ++gp) {
-                    const int c = pc >> 1, sub = pc & 1;
+                for (int pc = 0; pc < PIECES * CPG; ++pc, ++gp) {
+                    const int c = pc / PIECES, sub = pc % PIECES;
                     const uint32_t buf = (acc_it + c) & 1u;
                     const uint32_t use = (acc_it + c) >> 1;
                     const uint32_t sb = gp & 1u;
                     if (lane == 0) {
                         // the next piece (this tile's, or the first of the next tile)
-                        const bool last = pc + 1 == 2 * CPG;
+                        const bool last = pc + 1 == PIECES * CPG;
                         const int64_t mt_n = last ? mt + n_cl : mt;
                         if (mt_n < p.m_tiles) {
                             const int pn = last ? 0 : pc + 1;
                             bulk_wait_group_read0();  // that buffer's previous store has read it
                             mbar_arrive_expect_tx(&sh->hb_full[ew][sb ^ 1u], STAGE_BYTES);
                             tma_load_2d(stg0 + (sb ^ 1u) * STAGE_BYTES, &h_map, &sh->hb_full[ew][sb ^ 1u],
-                                        (int)(col0 + (pn >> 1) * BN + ch * 128 + (pn & 1) * 64), (int)(mt_n * BM + q * 32));
+                                        (int)(col0 + (pn / PIECES) * BN + piece_col(pn % PIECES)), (int)(mt_n * BM + q * 32));
                             loaded = gp + 2;
                         }
                     }
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {  // own row: 32 columns at a time
                         uint32_t y[32];
-                        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + ch * 128 + sub * 64 + half * 32, y);
+                        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + piece_col(sub) + half * 32, y);
                         tmem_ld_wait();
 #pragma unroll
                         for (int k4 = 0; k4 < 4; ++k4) {
@@ -312,11 +313,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     fence_proxy_async_smem();  // this thread's writes are visible to the TMA store
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&h_map, stg0 + sb * STAGE_BYTES, (int)(col0 + c * BN + ch * 128 + sub * 64),
+                        tma_store_2d(&h_map, stg0 + sb * STAGE_BYTES, (int)(col0 + c * BN + piece_col(sub)),
                                      (int)(m0 + q * 32));
                         bulk_commit_group();
                     }
-                    if (sub == 1) {
+                    if (sub == PIECES - 1) {
                         tc_fence_before();
                         if (lane == 0) {
                             mbar_arrive(&sh->acc_empty[buf]);
@@ -326,88 +327,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 acc_it += CPG;
                 if (!ok) break;
-                continue;
             }
-            // h = bf16(h + gate * y) on this warp's 32 rows and 128 columns of
-            // each chunk, in pieces of 64 columns, through the staging tile
-            // (16-byte chunk c of row r at chunk c ^ (r & 7)); the next piece's
-            // loads are in flight while this one is computed.
-            uint8_t *stg = stage_smem + ew * STAGE_BYTES;
-            const uint32_t stg_a = smem_u32(stg);
-            const int lr = lane >> 3, lc = lane & 7;  // coalesced role: row 4j + lr, 16-byte chunk lc
-            auto piece_ptr = [&](int pc, int j) -> uint16_t * {
-                const int64_t t = m0 + q * 32 + 4 * j + lr;
-                return p.h + t * p.d + col0 + (int64_t)(pc >> 1) * BN + ch * 128 + (pc & 1) * 64 + lc * 8;
-            };
-            auto row_live = [&](int j) -> bool { return m0 + q * 32 + 4 * j + lr < p.n_query; };
-            uint4 a[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                a[j] = row_live(j) ? *reinterpret_cast<const uint4 *>(piece_ptr(0, j)) : make_uint4(0, 0, 0, 0);
-            bool ok = true;
-            for (int pc = 0; pc < 2 * CPG; ++pc) {
-                const int c = pc >> 1, sub = pc & 1;
-                const uint32_t buf = (acc_it + c) & 1u;
-                const uint32_t use = (acc_it + c) >> 1;
-                if (sub == 0) {
-                    if (!mbar_wait(&sh->acc_full[buf], use & 1u, abort)) { ok = false; break; }
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {  // h piece -> staging (coalesced layout)
-                    const int r = 4 * j + lr;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stg_a + r * 128 + ((lc ^ (r & 7)) << 4)),
-                                 "r"(a[j].x), "r"(a[j].y), "r"(a[j].z), "r"(a[j].w)
-                                 : "memory");
-                }
-                if (pc + 1 < 2 * CPG) {  // next piece in flight during this one
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        a[j] = row_live(j) ? *reinterpret_cast<const uint4 *>(piece_ptr(pc + 1, j)) : make_uint4(0, 0, 0, 0);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {  // own row: 32 columns at a time
-                    uint32_t y[32];
-                    tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + ch * 128 + sub * 64 + half * 32, y);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const int cch = half * 4 + k4;
-                        const uint32_t addr = stg_a + lane * 128 + ((cch ^ (lane & 7)) << 4);
-                        uint32_t w[4];
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr) : "memory");
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float y0 = __uint_as_float(y[8 * k4 + 2 * k]);
-                            const float y1 = __uint_as_float(y[8 * k4 + 2 * k + 1]);
-                            w[k] = GATED ? pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])))
-                                         : pack_bf16x2(bf16_lo(w[k]) + y0, bf16_hi(w[k]) + y1);
-                        }
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
-                    }
-                }
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {  // staging -> h (coalesced)
-                    const int r = 4 * j + lr;
-                    uint4 o;
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w) : "r"(stg_a + r * 128 + ((lc ^ (r & 7)) << 4)) : "memory");
-                    if (row_live(j)) *reinterpret_cast<uint4 *>(piece_ptr(pc, j)) = o;
-                }
-                __syncwarp();
-                if (sub == 1) {
-                    tc_fence_before();
-                    if (lane == 0) {
-                        mbar_arrive(&sh->acc_empty[buf]);
-                        if (GATED && c == LEAD_CHUNK) mbar_arrive(&sh->upd_mark[pb]);
-                    }
-                }
-            }
-            acc_it += CPG;
-            if (!ok) break;
         }
-        if (kTmaUpdate && lane == 0) {
+        if (lane == 0) {
             bulk_wait_group0();  // stores complete before the CTA leaves
             int no_abort = 0;    // and no requested piece is still landing (after an abort)
             for (uint32_t k = gp; k < loaded; ++k)
