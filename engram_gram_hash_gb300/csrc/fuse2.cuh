@@ -5,7 +5,7 @@
 // (128 tokens x 64, 16 KB) beside the W block (64 x 256, 32 KB) it multiplies,
 // 3 stages of 48 KB; X is read from L2 once per 256-column chunk.  The
 // epilogue is split in two warp roles that run concurrently:
-//   - six gate warps reduce sum(h^2) and <h,g> over this CTA's d slice for
+//   - eight gate warps reduce sum(h^2) and <h,g> over this CTA's d slice for
 //     the tokens of the NEXT tile while the current one is being updated, and
 //     publish the partial sums to the cluster (double-buffered).  They start
 //     a tile once the update warps finish the previous tile's first chunk and
@@ -16,7 +16,7 @@
 //     32 x 64 pieces of h that come in and go out by TMA through two 128-byte
 //     swizzled staging buffers per warp, one piece landing while the other is
 //     updated.
-// Sixteen warps, four per scheduler, 128 registers each.
+// Eighteen warps (112 registers each).
 //
 // Partial sums per token are reduced in the same order as in fuse.cuh (lanes
 // over 16-byte pieces, a butterfly over the warp, then the G CTAs in rank
@@ -59,10 +59,10 @@ constexpr int UPDATE_WARPS = 8;  // warps 4..11: two per TMEM lane quadrant (4 m
 // chunk LEAD_CHUNK of tile i (-1: as soon as they start tile i).  A shorter
 // lead keeps the gate warps' h reads in L2 until the update warps re-read them.
 constexpr int LEAD_CHUNK = 0;
-constexpr int GATE_WARPS = 14 - UPDATE_WARPS;  // warps 2, 3 and 4 + UPDATE_WARPS .. 15
+constexpr int NUM_WARPS = 18;  // 8 gate warps (16 and 20 warps measured slower)
+constexpr int GATE_WARPS = NUM_WARPS - 2 - UPDATE_WARPS;  // warps 2, 3 and 4 + UPDATE_WARPS .. NUM_WARPS - 1
 constexpr int PIECES = 4 * 4 / UPDATE_WARPS;    // 64-column pieces of a chunk per update warp
 constexpr int NSTAGE = UPDATE_WARPS == 4 ? 4 : 3;  // ring stages that fit beside the staging buffers
-constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 
 struct Shared {
