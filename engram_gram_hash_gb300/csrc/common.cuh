@@ -291,8 +291,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_saddr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr) : "memory");
+// One arrival on the barrier at this CTA-local shared address in each of the
+// first n CTAs of the cluster, ordered after this thread's earlier memory
+// accesses for cluster-scope acquirers: one fence, then relaxed arrivals (a
+// release on every arrival costs a fence each).
+__device__ __forceinline__ void mbar_arrive_cluster_ranks(uint32_t local_saddr, int n) {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    for (int r = 0; r < n; ++r) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(r));
+        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+    }
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
     uint32_t ok;

@@ -314,7 +314,7 @@ __global__ void __maxnreg__(168)  // 10 warps: 3 share a sub-partition (16K regi
             __syncwarp();
             if (lane == 0) {
                 const uint32_t bar = smem_u32(&sh->gate_bar[pb]);
-                for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+                mbar_arrive_cluster_ranks(bar, p.groups);
             }
             if (!mbar_wait_cluster(&sh->gate_bar[pb], (it >> 1) & 1u, abort)) break;
             float ssum = 0.f, dsum = 0.f;

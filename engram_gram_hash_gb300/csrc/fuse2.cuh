@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {  // this warp is done with part[pb] of every CTA
                     const uint32_t bar = smem_u32(&sh->part_free[pb]);
-                    for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+                    mbar_arrive_cluster_ranks(bar, p.groups);
                     if (LEAD_CHUNK < 0 || LEAD_CHUNK >= CPG) mbar_arrive(&sh->upd_mark[pb]);
                 }
             }
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 const uint32_t bar = smem_u32(&sh->part_full[pb]);
-                for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+                mbar_arrive_cluster_ranks(bar, p.groups);
             }
         }
     }

@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 const uint32_t bar = smem_u32(&sh->gate_bar[pb]);
-                for (int r = 0; r < p.groups; ++r) mbar_arrive_remote(mapa_shared(bar, (uint32_t)r));
+                mbar_arrive_cluster_ranks(bar, p.groups);
             }
             if (!mbar_wait_cluster(&sh->gate_bar[pb], (it >> 1) & 1u, abort)) break;
             float ssum = 0.f, dsum = 0.f;
