@@ -65,12 +65,39 @@ def nominal_bytes_per_token(d):
     return 48 * 256 + 4 * d
 
 
+def _code_only(src):
+    """C/C++/CUDA source without comments and blank-line or spacing changes,
+    so that the hash below moves only when the code does (string literals
+    containing comment markers are kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(" ".join(line.split()) for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash():
+    """sha256 prefix of the kernel sources' code (comments and spacing aside):
+    the DRAM-traffic figures under profiles/ are used only while it matches."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "engram_gram_hash_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

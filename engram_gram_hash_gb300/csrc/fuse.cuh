@@ -15,8 +15,8 @@
 //
 // The gate of a token needs its whole h row, but each CTA only owns d/G
 // columns: each CTA reduces sum(h^2) and <h,g> over its slice, the partial
-// sums are exchanged through distributed shared memory (remote mbarrier
-// arrivals, cluster-scope acquire), and every CTA adds the G partials in the
+// sums are exchanged through distributed shared memory (one cluster
+// fence then relaxed remote mbarrier arrivals, cluster-scope acquire), and every CTA adds the G partials in the
 // same order, so all CTAs hold bit-identical gates before any CTA writes h.
 //
 // Memory access: eight epilogue warps (two per TMEM lane quadrant, each

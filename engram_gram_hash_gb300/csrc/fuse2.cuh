@@ -23,12 +23,16 @@
 // order), so both kernels produce bit-identical gates and h.
 //
 // Cluster protocol for the partial-sum buffer b (tiles alternate b = 0, 1):
-//   part_full[b]: one arrival from every gate warp of every CTA (release)
-//                 after it wrote its rows of part[b]; update warps wait on it
+//   part_full[b]: one arrival from every gate warp of every CTA after it
+//                 wrote its rows of part[b]; update warps wait on it
 //                 (cluster acquire) before reading part[b] of every CTA;
 //   part_free[b]: one arrival from every update warp of every CTA after it
 //                 read part[b] of every CTA; gate warps wait on it before
 //                 writing part[b] again, two tiles later.
+// Each signal is one cluster-scope fence followed by relaxed remote arrivals
+// (mbar_arrive_cluster_ranks): a release on each of the G arrivals would cost
+// a fence each, and those fences sat on the path from the gate pass to the
+// update.
 //
 // Sources: rohitghumare.com "guides/deepseek-v4-1-flash", sections "The
 // architecture" (Engram rows are added into the residual stream through a

@@ -7,7 +7,8 @@
 //      boxes of 128 tokens x 64 columns (128-byte swizzle);
 //   2. reduces sum(h^2) and <h,g> over the slice from shared memory and
 //      exchanges the partial sums with the cluster (distributed shared memory,
-//      remote mbarrier arrivals, cluster-scope acquire), so every CTA holds
+//      a cluster fence then relaxed remote mbarrier arrivals, cluster-scope
+//      acquire), so every CTA holds
 //      the same gate per token;
 //   3. applies h = bf16(h + gate * y) in place in shared memory, chunk by
 //      chunk as the tcgen05 accumulators (M=128, N=256, fp32 in TMEM,
