@@ -79,27 +79,6 @@ __device__ __forceinline__ uint4 ld_nc_na_v4(const void *p) {
     return r;
 }
 
-// 32-byte (one whole L2 sector) load and store per thread.  Volatile: they
-// keep program order with the rest of the epilogue (the loads are issued as a
-// batch before anything waits on them).
-__device__ __forceinline__ void ld_v8(const void *p, uint32_t (&r)[8]) {
-    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "l"(p)
-                 : "memory");
-}
-__device__ __forceinline__ void st_v8(void *p, const uint32_t (&r)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]),
-                 "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-
-// Ask the TMA engine to pull [p, p+bytes) into L2 (no shared memory used).
-// p 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
