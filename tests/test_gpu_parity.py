@@ -370,3 +370,34 @@ def test_full_size_forward(eg, name):
     check_h(h[qt], rh)
     del w, idx, mem, h
     torch.cuda.empty_cache()
+
+
+def test_large_every_token_parallel_oracle(eg):
+    """The large workload (131,072 query tokens, R = 8,388,608, d = 4096) at full
+    size through engram_forward, the call the benchmark times: mem and h on
+    EVERY query token against the oracle, which runs over all host cores in
+    spawned worker processes from the generators' host twins."""
+    import oracle_pool
+
+    cfg = CONFIGS["large"]
+    free, _ = torch.cuda.mem_get_info()
+    need = cfg.table_bytes * 1.02 + cfg.tq * (cfg.d * 2 * 2 + 512 * 8 + 48 * 8) + (1 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.1f} GB of device memory, {free / 1e9:.1f} GB free")
+    w = Workload(cfg)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets, last_n=cfg.last_n)
+    mem = eg.engram_gather_reduce(w.c, w.tables, w.scales, idx)
+    h = w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, last_n=cfg.last_n)
+    _clear(eg)
+    gm = mem.cpu().numpy()
+    gh = h.view(torch.int16).cpu().numpy().view(np.uint16)
+    args = (cfg, w.seeds, w.tok, w.offs, w.qpos)
+    del w, idx, mem, h
+    torch.cuda.empty_cache()
+    s = oracle_pool.check_all_tokens(*args, gm, gh)
+    print(f"\nevery-token oracle check: {s['tokens']} tokens in {s['seconds']:.1f} s on {s['procs']} processes "
+          f"({s['tokens'] / s['seconds']:.0f} tokens/s); worst mem {s['mem_worst']:.2e} x sum|term|, "
+          f"worst h {s['h_worst']:.2e}")
+    assert s["tokens"] == cfg.tq
+    assert s["mem_bad"] == 0 and s["h_bad"] == 0, s
