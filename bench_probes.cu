@@ -1,5 +1,5 @@
 // Bandwidth probes for bench.py --probe: the ceilings the Engram kernels are
-// judged against on this GPU.  Not part of libengram.
+// measured against on this GPU.  Not part of libengram.
 //  - random_rows: one warp reads 2 random 256-byte rows per load instruction
 //    (the gather's access pattern, 12 loads in flight per lane) from a buffer
 //    of n_rows rows, optionally with one 4-byte scale per row from a second
