@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <map>
+#include <atomic>
 #include <mutex>
 #include <cstdlib>
 #include <cstring>
@@ -567,17 +568,21 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
 
 // ================================================================ host side ==
 
+// Per-device host caches below are relaxed atomics: host threads that reach a
+// first call together compute and store the same value.
 int num_sms() {
-    static int sms[64] = {0};
+    static std::atomic<int> sms[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 148;
-    if (sms[dev] == 0) {
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         int v = 0;
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        sms[dev] = v > 0 ? v : 148;
+        n = v > 0 ? v : 148;
+        sms[dev].store(n, std::memory_order_relaxed);
     }
-    return sms[dev];
+    return n;
 }
 
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -802,15 +807,16 @@ enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X_GATE_WARPS = 2, FUSE_LAYER = 3 };
 // the tiles.  attr_done / max_clusters belong to one kernel instantiation.
 template <typename Kern, typename... Args>
 static engram_status launch_persistent(Kern kern, int threads, int smem, int groups, int64_t m_tiles,
-                                       bool *attr_done, int (*max_clusters)[fuse::MAX_GROUPS + 1], cudaStream_t st,
+                                       std::atomic<bool> *attr_done,
+                                       std::atomic<int> (*max_clusters)[fuse::MAX_GROUPS + 1], cudaStream_t st,
                                        const Args &...args) {
     int dev = 0;
     cudaGetDevice(&dev);
     const bool cache = dev >= 0 && dev < 64;
-    if (!cache || !attr_done[dev]) {
+    if (!cache || !attr_done[dev].load(std::memory_order_relaxed)) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fuse smem)");
-        if (cache) attr_done[dev] = true;
+        if (cache) attr_done[dev].store(true, std::memory_order_relaxed);
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -823,7 +829,7 @@ static engram_status launch_persistent(Kern kern, int threads, int smem, int gro
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int mc = cache ? max_clusters[dev][groups] : 0;
+    int mc = cache ? max_clusters[dev][groups].load(std::memory_order_relaxed) : 0;
     if (mc == 0) {
         cfg.gridDim = dim3(groups * 64);
         int n = 0;
@@ -832,7 +838,7 @@ static engram_status launch_persistent(Kern kern, int threads, int smem, int gro
             n = num_sms() / groups;
         }
         mc = n;
-        if (cache) max_clusters[dev][groups] = n;
+        if (cache) max_clusters[dev][groups].store(n, std::memory_order_relaxed);
     }
     const int64_t clusters = std::min<int64_t>(m_tiles, mc);
     cfg.gridDim = dim3((unsigned)(clusters * groups));
@@ -857,8 +863,8 @@ static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &x
     constexpr bool k2 = KIND == FUSE_BF16_X_GATE_WARPS || KIND == FUSE_LAYER;
     constexpr int kThreads = k2 ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
     constexpr int kSmem = k2 ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
-    static bool attr_done[64] = {};
-    static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
+    static std::atomic<bool> attr_done[64] = {};
+    static std::atomic<int> max_clusters[64][fuse::MAX_GROUPS + 1] = {};
     if constexpr (k2)
         return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
                                  max_clusters, st, wmap, xmap, hmap, p);
@@ -883,8 +889,8 @@ static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &x
 template <int CPG>
 static engram_status fuse3_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hl,
                                     const CUtensorMap &hs, const fuse::Params &p, cudaStream_t st) {
-    static bool attr_done[64] = {};
-    static int max_clusters[64][fuse::MAX_GROUPS + 1] = {};
+    static std::atomic<bool> attr_done[64] = {};
+    static std::atomic<int> max_clusters[64][fuse::MAX_GROUPS + 1] = {};
     return launch_persistent(fuse3::fuse3_kernel<CPG>, fuse3::NUM_THREADS, fuse3::smem_bytes<CPG>(), p.groups,
                              p.m_tiles, attr_done, max_clusters, st, wmap, xmap, hl, hs, p);
 }
@@ -992,13 +998,13 @@ static engram_status query_launch(const engram_config *cfg, const uint16_t *A, i
     if (!bf16_map_2d(&bmap, B, kLayerWidth, (uint64_t)K, 64, layer::BK))
         return cuda_fail(cudaErrorInvalidValue, "query B map");
     auto kern = layer::query_kernel<RMS, SPLIT>;
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, layer::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(query smem)");
-        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
     }
     const unsigned grid = (unsigned)std::min<int64_t>(p.m_tiles, num_sms());
     kern<<<grid, layer::NUM_THREADS, layer::SMEM_BYTES, st>>>(amap, bmap, p);
