@@ -116,6 +116,35 @@ def test_invalid_arguments_rejected_before_any_device_work(eg):
                             ctypes.c_void_p(256), 100, ctypes.c_void_p(256), ctypes.c_void_p(256), null) == 6
 
 
+def test_layer_entry_points_check_arguments_before_device_work(eg):
+    """engram_layer_keys / engram_layer_forward reject bad arguments with a
+    status before any CUDA call (the fake pointers below are never touched)."""
+    lib = eg.lib()
+    from synth.configs import default_seeds
+
+    P = ctypes.c_void_p
+    a = P(256)  # aligned stand-in, never dereferenced
+    c = eg.make_config(1024, 4096, 256, default_seeds())
+    assert lib.engram_layer_keys(ctypes.byref(c), None, a, None) == 1
+    assert lib.engram_layer_keys(ctypes.byref(c), P(258), a, None) == 1  # misaligned W_k
+    n = 1000
+    assert eg.engram_layer_workspace_bytes(c, n) >= n * (512 * 2 + 256 * 4 + 256 * 2)
+
+    def fwd(cfg, module=0, n_seqs=1, last_n=0, n_query=4, tables=a, ws_bytes=1 << 30):
+        return lib.engram_layer_forward(ctypes.byref(cfg), module, a, a, n_seqs, last_n, n_query, tables, a, a, a, a,
+                                        a, a, ws_bytes, None)
+
+    assert fwd(c, module=2) == 1                        # module 0 or 1
+    assert fwd(c, n_query=0) == 0                       # nothing to do
+    assert fwd(c, tables=None) == 1                     # null tables
+    assert fwd(c, n_seqs=2, last_n=1, n_query=4) == 1   # n_query != n_seqs * last_n
+    assert fwd(c, ws_bytes=16) == 6                     # workspace too small
+    c_mx = eg.make_config(1024, 4096, 256, default_seeds(), row_layout=eg.ROWS_MX)
+    assert fwd(c_mx) == 7                               # MX rows: not in the per-layer form
+    c_d = eg.make_config(1024, 4096, 320, default_seeds())
+    assert fwd(c_d) == 1                                # d not a multiple of 256
+
+
 def test_product_path_does_not_import_the_oracle():
     """The binding and the CUDA sources never reference oracle/."""
     pkg = os.path.join(ROOT, "engram_gram_hash_gb300")
