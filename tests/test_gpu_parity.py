@@ -372,14 +372,17 @@ def test_full_size_forward(eg, name):
     torch.cuda.empty_cache()
 
 
-def test_large_every_token_parallel_oracle(eg):
-    """The large workload (131,072 query tokens, R = 8,388,608, d = 4096) at full
-    size through engram_forward, the call the benchmark times: mem and h on
-    EVERY query token against the oracle, which runs over all host cores in
-    spawned worker processes from the generators' host twins."""
+@pytest.mark.parametrize("name", ["large", "prefill"])
+def test_every_token_parallel_oracle(eg, name):
+    """The large workload (131,072 query tokens, uniform ids, R = 8,388,608) and
+    the prefill workload (8 x 32,768 tokens, Zipf ids with repeated spans,
+    R = 2,097,152), d = 4096, at full size through engram_forward, the call the
+    benchmark times: mem and h on EVERY query token against the oracle, which
+    runs over all host cores in spawned worker processes from the generators'
+    host twins."""
     import oracle_pool
 
-    cfg = CONFIGS["large"]
+    cfg = CONFIGS[name]
     free, _ = torch.cuda.mem_get_info()
     need = cfg.table_bytes * 1.02 + cfg.tq * (cfg.d * 2 * 2 + 512 * 8 + 48 * 8) + (1 << 30)
     if free < need:
