@@ -16,7 +16,7 @@
 //     32 x 64 pieces of h that come in and go out by TMA through two 128-byte
 //     swizzled staging buffers per warp, one piece landing while the other is
 //     updated.
-// Eighteen warps (112 registers each).
+// Eighteen warps, one CTA per SM (at most 112 registers a thread; 96 used).
 //
 // Partial sums per token are reduced in the same order as in fuse.cuh (lanes
 // over 16-byte pieces, a butterfly over the warp, then the G CTAs in rank
