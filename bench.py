@@ -49,20 +49,31 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
 
 
-# Algorithmic bytes per query token of each kernel (what the method must move):
-#   gather: 4 B of token id + 48 x 256 B of rows + 48 x 4 B of scales in, 512 x 2 B of X out
-#   fuse:   512 x 2 B of X in, d x 2 B of h in, d x 2 B of h out
+# Algorithmic bytes per query token (what the method must move, as the
+# measurement plan counts them): 48 rows of 256 code bytes plus their scales
+# for the gather, the residual read and write (4 d bytes) for the projection.
+# The bf16 X handed between the two kernels (1 KB each way), the token id and
+# the scale bytes fetched beyond the 4 used are reported apart.
 def kernel_bytes_per_token(d, layout="separate"):
-    """Algorithmic bytes per query token: the gather reads one token id, 48 rows
-    of 256 code bytes plus their scales (one fp32, or eight E8M0 bytes for MX
-    rows) and writes 512 bf16; the fuse reads X and h and writes h."""
+    """Algorithmic bytes per query token of each kernel: the gather reads 48
+    rows of 256 code bytes plus their scales (one fp32, or eight E8M0 bytes
+    for MX rows); the projection reads and writes the bf16 residual h."""
     scale = 8 if layout == "mx" else 4
-    return {"gather": 4 + 48 * (256 + scale) + 512 * 2, "fuse": 512 * 2 + 4 * d}
+    return {"gather": 48 * (256 + scale), "fuse": 4 * d}
+
+
+def handoff_bytes_per_token():
+    """Bytes per query token outside the method's count: the bf16 X written by
+    the gather and read by the projection, and the token id."""
+    return {"X_write": 512 * 2, "X_read": 512 * 2, "token": 4}
 
 
 def nominal_bytes_per_token(d):
     """The path's nominal bytes: 48 rows of 256 B plus the residual read and write."""
     return 48 * 256 + 4 * d
+
+
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, for context beside the measured copy peak
 
 
 def _code_only(src):
@@ -127,20 +138,72 @@ def smi_index(local_rank):
     return str(local_rank)
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver): SM clock, its maximum, and the active clock-event reasons."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(int(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML device")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct = self.ct
+        mhz, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz))  # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return time.time(), float(mhz.value), float(mx.value), [n for b, n in self.REASONS.items() if rs.value & b]
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """SM clocks and throttle reasons sampled during the timed region: every
+    2 ms through NVML in a thread (read-only queries), or every 100 ms from
+    nvidia-smi where NVML cannot be loaded."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_s=0.002):
         self.gpu = gpu_index
+        self.period = period_s
         self.proc = None
+        self.nvml = None
+        self.rows = []
         self.path = os.path.join("/tmp", f"engram_clocks_{os.getpid()}.csv")
         self.t_start = self.t_end = None
 
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                self.rows.append(self.nvml.sample())
+            except OSError:
+                break
+            self._stop.wait(self.period)
+
     def __enter__(self):
+        import threading
+
+        try:
+            self.nvml = _Nvml(self.gpu)
+            self._stop = threading.Event()
+            self._thr = threading.Thread(target=self._loop, daemon=True)
+            self._thr.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -160,6 +223,9 @@ class ClockSampler:
         self.t_end = time.time()
 
     def __exit__(self, *a):
+        if self.nvml is not None:
+            self._stop.set()
+            self._thr.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -168,9 +234,7 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _smi_rows(self):
         from datetime import datetime
 
         rows = []
@@ -187,17 +251,27 @@ class ClockSampler:
                 except ValueError:
                     continue
         os.unlink(self.path)
+        return rows
+
+    def summary(self):
+        if self.nvml is not None:
+            rows, src = self.rows, "nvml every 2 ms"
+        elif self.proc is not None and os.path.exists(self.path):
+            rows, src = self._smi_rows(), "nvidia-smi every 100 ms"
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": src}
         window = "timed region"
-        sel = [r for r in rows if self.t_start is not None and self.t_start - 0.05 <= r[0] <= self.t_end + 0.05]
+        sel = [r for r in rows if self.t_start is not None and self.t_start - 0.002 <= r[0] <= self.t_end + 0.002]
         if len(sel) < 2:  # a timed region shorter than the sampling period: use the nearest samples
-            window = "timed region too short for 100 ms sampling; samples nearest to it"
+            window = "timed region shorter than the sampling period; samples nearest to it"
             mid = 0.5 * (self.t_start + self.t_end) if self.t_start else rows[-1][0]
             sel = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
         reasons = sorted({x for r in sel for x in r[3]})
         return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
-                "reasons": reasons, "samples": len(sel), "window": window}
+                "sm_mhz_min": min(r[1] for r in sel), "reasons": reasons, "samples": len(sel), "window": window,
+                "source": src}
 
 
 # ------------------------------------------------------ multi-rank pieces ----
@@ -313,7 +387,10 @@ def run_ours(args, rank, world, local_rank):
     if args.tokens:
         base = base.with_(seq_lens=tuple(min(L, args.tokens) for L in base.seq_lens))
     # weak scaling: rank r draws its own token batch (tables are replicated weights)
-    cfg = rank_config(base, rank)
+    sharded = args.shard == "rows"
+    # weak scaling: every rank its own batch; row-sharded tables: one batch on
+    # every rank (each rank holds 1/world of every table's rows)
+    cfg = base if sharded else rank_config(base, rank)
     seeds = default_seeds()
     record = args.layout != "separate"  # rows carry their scales (fp32, or MX block scales)
     c = eg.make_config(cfg.V, cfg.R, cfg.d, seeds, cfg.rms_eps,
@@ -325,20 +402,36 @@ def run_ours(args, rank, world, local_rank):
     rb = eg.RECORD_BYTES if record else 256
     kw = {"pin_memory": True} if cfg.host_tables else {"device": dev}
     huge = cfg.host_tables and args.host_alloc == "huge"
-    if huge:  # pinned, on transparent huge pages (engram_host_alloc), zeroed
+    if sharded and (cfg.host_tables or args.layout != "separate" or args.variant != "concat"):
+        raise SystemExit("--shard rows runs the concatenated form on HBM tables with fp32 row scales")
+    if sharded:  # this rank's rows r = rank + k * world of every table, generated one table at a time
+        rows_per = eg.engram_shard_rows(c, world)
+        tables = torch.zeros((48, rows_per, 256), dtype=torch.uint8, device=dev)
+        scales = torch.zeros((48, rows_per), dtype=torch.float32, device=dev)
+        tmp_t = torch.empty((1, cfg.R, 256), dtype=torch.uint8, device=dev)
+        tmp_s = torch.empty((1, cfg.R), dtype=torch.float32, device=dev)
+        for j in range(48):
+            sd.fill_tables(tmp_t, base.seed, j0=j)
+            sd.fill_scales(tmp_s, base.seed, j0=j)
+            mine_t, mine_s = tmp_t[0, rank::world], tmp_s[0, rank::world]
+            tables[j, :mine_t.shape[0]] = mine_t
+            scales[j, :mine_s.shape[0]] = mine_s
+        del tmp_t, tmp_s
+    elif huge:  # pinned, on transparent huge pages (engram_host_alloc), zeroed
         tables = eg.host_tables_empty((48, cfg.R, rb), torch.uint8)
     else:
         tables = torch.zeros((48, cfg.R, rb), dtype=torch.uint8, **kw)
-    sd.fill_tables(tables, base.seed)
-    scales = None
-    if args.layout == "mx":
-        sd.fill_mx_scales(tables, base.seed)
-    elif record:
-        sd.fill_record_scales(tables, base.seed)
-    else:
-        scales = (eg.host_tables_empty((48, cfg.R), torch.float32) if huge
-                  else torch.empty((48, cfg.R), dtype=torch.float32, **kw))
-        sd.fill_scales(scales, base.seed)
+    if not sharded:
+        sd.fill_tables(tables, base.seed)
+        scales = None
+        if args.layout == "mx":
+            sd.fill_mx_scales(tables, base.seed)
+        elif record:
+            sd.fill_record_scales(tables, base.seed)
+        else:
+            scales = (eg.host_tables_empty((48, cfg.R), torch.float32) if huge
+                      else torch.empty((48, cfg.R), dtype=torch.float32, **kw))
+            sd.fill_scales(scales, base.seed)
     W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=dev)
     g = torch.empty(cfg.d, dtype=torch.bfloat16, device=dev)
     h = torch.empty((cfg.tq, cfg.d), dtype=torch.bfloat16, device=dev)
@@ -370,35 +463,58 @@ def run_ours(args, rank, world, local_rank):
         n_unique = torch.zeros(1, dtype=torch.int64, device=dev)
         side = torch.cuda.Stream(device=dev)
         ev_a, ev_b = torch.cuda.Event(), torch.cuda.Event()
+    elif sharded:
+        from engram_gram_hash_gb300 import shard as eshard
 
-    def step(ev=None):
+        mem = torch.empty((nq, 512), dtype=torch.float32, device=dev)
+    elif not layers:
+        fws = torch.empty(eg.engram_forward_workspace_bytes(c, nq), dtype=torch.uint8, device=dev)
+
+    def step():
+        """One pass of the whole path; returns the kernels it launched."""
         if host:
-            if ev is not None:
-                ev[0].record(stream)
             eg.engram_forward_host(c, tokens, seq_offsets, tables, scales, W, g, h, cap, last_n=cfg.last_n,
                                    n_query=nq, workspace=fws, n_unique=n_unique, side_stream=side, ev_dedup=ev_a,
                                    ev_staged=ev_b)
-            if ev is not None:
-                ev[1].record(stream)
             return 9  # hash, 5 dedup kernels, stage, staged gather, fuse
         if layers:
             for m in (0, 1):
-                if ev is not None:
-                    ev[m].record(stream)
                 eg.engram_layer_forward(c, m, tokens, seq_offsets, tables, scales, lw[m][0], lw[m][1], lw[m][2], h,
                                         last_n=cfg.last_n, n_query=nq, workspace=lws)
-            if ev is not None:
-                ev[2].record(stream)
             return 8  # per layer: query, key-side query, gated gather, projection
-        if ev is not None:
-            ev[0].record(stream)
-        eg.engram_gather_x(c, tokens, seq_offsets, tables, scales, last_n=cfg.last_n, n_query=nq, X=X)
-        if ev is not None:
-            ev[1].record(stream)
-        eg.engram_fuse_x(c, X, W, g, h)
-        if ev is not None:
-            ev[2].record(stream)
+        if sharded:  # partial gather of this rank's rows, all-reduce of mem, projection
+            eshard.forward_row_sharded(c, rank, world, tokens, seq_offsets, tables, scales, W, g, h,
+                                       last_n=cfg.last_n, n_query=nq, mem=mem)
+            return 2
+        # engram_forward: the gather kernel, then the projection launched as its
+        # programmatic dependent (its gate pass starts while the gather drains)
+        eg.engram_forward(c, tokens, seq_offsets, tables, scales, W, g, h, last_n=cfg.last_n, n_query=nq,
+                          workspace=fws)
         return 2
+
+    def split_step(ev):
+        """The same pass with CUDA events between its kernels (for the
+        per-kernel times; the events keep the kernels apart)."""
+        if layers:
+            for m in (0, 1):
+                ev[m].record(stream)
+                eg.engram_layer_forward(c, m, tokens, seq_offsets, tables, scales, lw[m][0], lw[m][1], lw[m][2], h,
+                                        last_n=cfg.last_n, n_query=nq, workspace=lws)
+            ev[2].record(stream)
+            return
+        ev[0].record(stream)
+        if sharded:
+            eg.engram_gather_reduce_shard(c, rank, world, tokens, seq_offsets, tables, scales, last_n=cfg.last_n,
+                                          n_query=nq, mem=mem)
+            eshard.reduce_partials(mem)
+        else:
+            eg.engram_gather_x(c, tokens, seq_offsets, tables, scales, last_n=cfg.last_n, n_query=nq, X=X)
+        ev[1].record(stream)
+        if sharded:
+            eg.engram_fuse(c, mem, W, g, h)
+        else:
+            eg.engram_fuse_x(c, X, W, g, h)
+        ev[2].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -407,7 +523,6 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device error during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     with ClockSampler(smi_index(local_rank)) as cs:
@@ -417,7 +532,7 @@ def run_ours(args, rank, world, local_rank):
         cs.mark_start()
         t0.record(stream)
         for k in range(K):
-            launches += step(evs[k])
+            launches += step()
         t1.record(stream)
         torch.cuda.synchronize()
         cs.mark_end()
@@ -427,8 +542,25 @@ def run_ours(args, rank, world, local_rank):
     status = eg.engram_last_error()
     if status != 0:
         raise RuntimeError(f"device error {status} in the timed region")
-    value, ms_max = job_rate(ms, K, cfg.tq, world, dev)
+    # whole-job tokens per step: every rank's batch, or the one shared batch when sharded
+    value, ms_max = job_rate(ms, K, cfg.tq / world if sharded else cfg.tq, world, dev)
     clocks = cs.summary()
+    if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        clocks["time_x_median_mhz"] = round(ms / K * clocks["sm_mhz"], 2)  # ms x MHz, for comparing runs
+
+    # per-kernel times: a separate pass with events between the kernels
+    per_kernel_ms = {}
+    if not host:
+        KS = max(3, min(K, 20))
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KS)]
+        for k in range(KS):
+            split_step(evs[k])
+        torch.cuda.synchronize()
+        if eg.engram_last_error() != 0:
+            raise RuntimeError("device error in the per-kernel pass")
+        names = ("layer0", "layer1") if layers else ("gather", "fuse")
+        per_kernel_ms = {names[0]: sum(e[0].elapsed_time(e[1]) for e in evs) / KS,
+                         names[1]: sum(e[1].elapsed_time(e[2]) for e in evs) / KS}
 
     # What stays in L2 between timed steps (129 MB): tables are always far larger;
     # a small batch's h and W_out are not.
@@ -442,24 +574,22 @@ def run_ours(args, rank, world, local_rank):
                                         max(K, 200))
 
     peaks = measured_peaks()
-    per_kernel_ms = {}
-    if layers:
-        per_kernel_ms = {
-            "layer0": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
-            "layer1": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
-        }
-    elif not host:
-        per_kernel_ms = {
-            "gather": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
-            "fuse": sum(e[1].elapsed_time(e[2]) for e in evs) / K,
-        }
     # algorithmic bytes per token; a layer moves its 24 rows + scales and h once each way
-    kb = ({"layer0": 4 + 24 * 260 + 4 * cfg.d, "layer1": 4 + 24 * 260 + 4 * cfg.d} if layers
+    kb = ({"layer0": 24 * 260 + 4 * cfg.d, "layer1": 24 * 260 + 4 * cfg.d} if layers
           else kernel_bytes_per_token(cfg.d, args.layout))
+    if sharded:  # this rank's share of the rows; the fp32 mem is written, exchanged and read
+        kb = {"gather": -(-48 * 260 // world), "fuse": 4 * cfg.d}
     kernels = {}
     for name, kms in per_kernel_ms.items():
         gbs = kb[name] * nq / (kms * 1e-3) / 1e9
-        kernels[name] = {"ms": round(kms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 3)}
+        kernels[name] = {"ms": round(kms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 3),
+                         "algorithmic_bytes_per_token": kb[name]}
+    if not layers and not host and not sharded:
+        hb = handoff_bytes_per_token()
+        kernels["gather"]["also_moved_per_token"] = {"X_write": hb["X_write"], "token": hb["token"],
+                                                     "scale_sector_bytes_beyond_used": 48 * (32 - 4)}
+        kernels["fuse"]["also_moved_per_token"] = {"X_read": hb["X_read"]}
+        kernels["pdl_overlap_ms"] = round(sum(per_kernel_ms.values()) - ms / K, 4)
     roofline = None
     if per_kernel_ms:
         dom = max(per_kernel_ms, key=per_kernel_ms.get)
@@ -468,16 +598,21 @@ def run_ours(args, rank, world, local_rank):
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": tr,
                     "algorithmic_bytes_per_launch": kb[dom] * nq,
-                    "peak_src": f"{peaks['src']} hbm_gbs (burst copy)"}
+                    "peak_src": f"{peaks['src']} hbm_gbs (burst copy)",
+                    "frac_vs_nominal_7900": round(ach / NOMINAL_HBM_GBS, 4)}
 
     if host:
         roofline = host_link_roofline(eg, c, cfg, tokens, seq_offsets, tables, scales, nq, dev)
 
     nominal = 2 * (24 * 256 + 4 * cfg.d) if layers else nominal_bytes_per_token(cfg.d)
     step_gbs = nominal * nq / (ms_max * 1e-3 / K) / 1e9
+    step_roofline = {"nominal_bytes_per_token": nominal, "achieved_GBps": round(step_gbs, 1),
+                     "peak_GBps": peaks["hbm_gbs"], "frac": round(step_gbs / peaks["hbm_gbs"], 4),
+                     "frac_vs_nominal_7900": round(step_gbs / NOMINAL_HBM_GBS, 4)}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "strong" if sharded else "weak",
+        "vs_baseline": None,
         "dtype": "e4m3->f32 gather, bf16 x bf16 -> f32 projection, bf16 residual",
         "data": ("synthetic (seeded; tables e4m3 ~ quantised N(0,1), "
                  + ("E8M0 block scales 2^-2..2^2 per 32 codes)" if args.layout == "mx"
@@ -489,9 +624,10 @@ def run_ours(args, rank, world, local_rank):
                                   "mx": "272-byte MX records: 256 e4m3 codes + 8 E8M0 block scales",
                                   "separate": "256-byte rows + separate fp32 scale array"}[args.layout],
                    "token_ids": ("uniform" if cfg.zipf_s == 0 else f"Zipf({cfg.zipf_s})"),
-                   "l2": l2_note, "parallelism": f"dp{world} (replicated tables)"},
-        "step_roofline": {"nominal_bytes_per_token": nominal, "achieved_GBps": round(step_gbs, 1),
-                          "peak_GBps": peaks["hbm_gbs"], "frac": round(step_gbs / peaks["hbm_gbs"], 4)},
+                   "l2": l2_note,
+                   "parallelism": (f"row-sharded tables over {world} rank(s), all-reduce of mem" if sharded
+                                   else f"dp{world} (replicated tables)")},
+        "step_roofline": step_roofline,
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clocks,
     }
     if layers:
@@ -508,9 +644,9 @@ def run_ours(args, rank, world, local_rank):
         out["pipelined"] = [time_host_pipelined(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
                                                 ch, max(3, min(K, 20)))
                             for ch in args.host_chunks if 0 < ch < nq]
-    if not args.no_e2e and not layers:
+    if not args.no_e2e and not layers and not sharded:
         out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not layers:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not layers and not sharded:
         out["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     return out
 
@@ -652,25 +788,56 @@ def oracle_sample_tokens_per_s(cfg, seconds, seed=0):
     return done_t / done_s, done_t, done_s
 
 
+def _oracle_job(job):
+    """Pool worker (spawned): the oracle's tokens/s on its own random sample."""
+    cfg, seconds, seed = job
+    _, n, secs = oracle_sample_tokens_per_s(cfg, seconds, seed=seed)
+    return n, secs
+
+
+def oracle_pool(procs):
+    """A pool of `procs` spawned processes (never forked: the parent may hold
+    a CUDA context)."""
+    import multiprocessing as mp
+
+    return mp.get_context("spawn").Pool(procs)
+
+
+def oracle_all_cores(cfg, seconds, pool, procs, seed0):
+    """The same oracle on `procs` worker processes at once (one per host
+    core), each on its own random sample for ~`seconds` of CPU.  Returns
+    (aggregate tokens/s = sum of the workers' rates, tokens, the slowest
+    worker's oracle seconds)."""
+    res = pool.map(_oracle_job, [(cfg, seconds, seed0 + i) for i in range(procs)], chunksize=1)
+    return sum(n / s for n, s in res), sum(n for n, _ in res), max(s for _, s in res)
+
+
 def cpu_baseline(cfg, seconds):
-    v, n, s = oracle_sample_tokens_per_s(cfg, seconds)
-    return {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} query tokens of the {cfg.name} workload drawn at random ({s:.1f} s single-threaded; "
-                      "hash + gather + fuse, input draws untimed)"}
+    """The oracle on the host: all cores at once (the value) and one core."""
+    nproc = os.cpu_count() or 1
+    v1, n1, s1 = oracle_sample_tokens_per_s(cfg, seconds)
+    with oracle_pool(nproc) as pool:
+        va, na, sa = oracle_all_cores(cfg, max(2.0, seconds / 2), pool, nproc, 1000)
+    return {"value": round(va, 2), "unit": UNIT, "cores": nproc, "kind": "oracle", "box_cores": nproc,
+            "sample": f"{na} query tokens of the {cfg.name} workload drawn at random, {nproc} spawned processes "
+                      f"at once (~{sa:.1f} s each; hash + gather + fuse, input draws untimed)",
+            "single_core": {"value": round(v1, 2), "cores": 1,
+                            "sample": f"{n1} query tokens, {s1:.1f} s single-threaded"}}
 
 
 def run_reference(args, rank, world):
     from synth.configs import CONFIGS
 
     cfg = CONFIGS[args.workload]
+    nproc = os.cpu_count() or 1
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
-    for _ in range(args.warmup):
-        oracle_sample_tokens_per_s(cfg, 0.2)
     total_t, total_s = 0, 0.0
-    for k in range(args.steps):
-        v, n, s = oracle_sample_tokens_per_s(cfg, per_step, seed=k + 1)
-        total_t += n
-        total_s += s
+    with oracle_pool(nproc) as pool:
+        oracle_all_cores(cfg, 0.2, pool, nproc, 0)  # warm-up: workers start, oracle loads
+        for k in range(args.steps):
+            v, n, s = oracle_all_cores(cfg, per_step, pool, nproc, 1000 * (k + 1))
+            total_t += n
+            total_s += n / v  # this step's tokens at its aggregate rate
     value = total_t / total_s
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -678,9 +845,10 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
         "data": "synthetic (seeded)", "config": {"workload": args.workload, "V": cfg.V, "R": cfg.R, "d_model": cfg.d,
                                                   "query_tokens_per_step_per_gpu": cfg.tq},
-        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{total_t} query tokens over {args.steps} steps, single-threaded, "
-                                   "each step a random sample of the workload"},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": nproc, "kind": "oracle",
+                         "box_cores": nproc,
+                         "sample": f"{total_t} query tokens over {args.steps} steps, {nproc} spawned processes "
+                                   "at once, each step a random sample of the workload per process"},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -722,6 +890,20 @@ def run_probe(args):
     return out
 
 
+def launch_ranks(n, argv=None):
+    """Start this script once per GPU under torch.distributed.run on this node
+    (rendezvous on 127.0.0.1); returns the launcher's exit code.  Rank 0
+    prints the JSON line."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)]
+    return subprocess.call(cmd + list(sys.argv[1:] if argv is None else argv))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -732,6 +914,9 @@ def main():
     ap.add_argument("--variant", default="concat", choices=["concat", "layers"],
                     help="concat: one [T,512] projection with a token gate (the headline path); layers: two "
                          "Engram layers with per-row gates")
+    ap.add_argument("--shard", default="none", choices=["none", "rows"],
+                    help="rows: every rank holds 1/N of every table's rows, gathers its share for one shared "
+                         "batch, and the partial sums are all-reduced before the projection")
     ap.add_argument("--layout", default="separate", choices=["record", "separate", "mx"],
                     help="table rows that carry their fp32 scale (record), MXFP8-style rows with eight E8M0 "
                          "block scales (mx), or a separate scale array")
@@ -750,7 +935,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3  # at least three warm-up steps
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1 and not args.probe:
+        sys.exit(launch_ranks(args.gpus))  # one process per GPU, then this script in each
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus and not args.probe:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one rank per GPU "
+                 f"(torch.distributed.run --nproc-per-node {args.gpus})")
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 

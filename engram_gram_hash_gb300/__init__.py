@@ -91,6 +91,8 @@ def lib():
             "engram_forward": ([C, P, P, i64, i32, i64, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "engram_gather_x": ([C, P, P, i64, i32, i64, P, P, P, P], ctypes.c_int),
             "engram_fuse_x": ([C, P, P, P, P, i64, P], ctypes.c_int),
+            "engram_shard_rows": ([C, i32], i64),
+            "engram_gather_reduce_shard": ([C, i32, i32, P, P, i64, i32, i64, P, P, P, P], ctypes.c_int),
             "engram_forward_no_workspace": ([C, P, P, i64, i32, i64, P, P, P, P, P, P], ctypes.c_int),
             "engram_dedup_workspace_bytes": ([C], sz),
             "engram_dedup": ([C, P, i64, P, sz, P, i64, P, P, P], ctypes.c_int),
@@ -412,6 +414,32 @@ def engram_fuse_x(cfg, X, W_out, g, h, stream=None):
         "engram_fuse_x",
     )
     return h
+
+
+def engram_shard_rows(cfg, n_shards):
+    """Rows per table held by each of n_shards row shards: ceil(R / n_shards)."""
+    return int(lib().engram_shard_rows(ctypes.byref(cfg), int(n_shards)))
+
+
+def engram_gather_reduce_shard(cfg, shard, n_shards, tokens, seq_offsets, tables_shard, scales_shard, last_n=0,
+                               n_query=None, mem=None, stream=None):
+    """This row shard's partial module sums, fp32 [n_query, 512] (rows owned
+    by other shards add nothing); the sum over shards is the whole mem."""
+    _need(tokens, torch.int32, "tokens")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(tables_shard, torch.uint8, "tables")
+    _need(scales_shard, torch.float32, "scales")
+    nq = _n_query(tokens, seq_offsets, last_n, n_query)
+    if mem is None:
+        mem = torch.empty((nq, MEM_DIM), dtype=torch.float32, device=tokens.device)
+    _need(mem, torch.float32, "mem")
+    _check(
+        lib().engram_gather_reduce_shard(ctypes.byref(cfg), int(shard), int(n_shards), _ptr(tokens),
+                                         _ptr(seq_offsets), seq_offsets.numel() - 1, last_n, nq, _ptr(tables_shard),
+                                         _ptr(scales_shard), _ptr(mem), _stream(stream)),
+        "engram_gather_reduce_shard",
+    )
+    return mem
 
 
 def engram_dedup_workspace_bytes(cfg):

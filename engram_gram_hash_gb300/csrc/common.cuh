@@ -27,6 +27,14 @@ __device__ unsigned int g_error_word = 0;
 
 __device__ __forceinline__ void raise_error(engram_status st) { atomicOr(&g_error_word, 1u << (int)st); }
 
+// Programmatic dependent launch.  allow_dependent_launch: a grid launched
+// with a programmatic dependency on this one may start once every CTA of this
+// grid has executed it (or exited).  grid_dependency_wait: the calling thread
+// waits until the grids this one depends on have completed and their memory
+// writes are visible; without a programmatic dependency it returns at once.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

@@ -128,7 +128,12 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
 // projection's operand; bf16 rounding of the same fp32 sums, so both outputs
 // agree bit for bit after rounding).
 
-enum IdxMode { IDX_I64 = 0, IDX_STAGED_I32 = 1, IDX_HASH = 2 };
+// IDX_HASH_SHARD: hashed in registers, but only the rows this shard owns
+// are read (row r of every table belongs to shard r mod n_shards, stored
+// there as local row r / n_shards); the others add nothing.
+enum IdxMode { IDX_I64 = 0, IDX_STAGED_I32 = 1, IDX_HASH = 2, IDX_HASH_SHARD = 3 };
+
+constexpr int32_t kSlotNone = -1;  // idx_staged entry that names no staged row
 
 enum ScaleMode { SCALE_ARRAY = 0, SCALE_IN_ROW = 1, SCALE_MX = 2 };
 
@@ -140,7 +145,10 @@ struct GatherParams {
     int64_t n_query;
     int64_t R;           // rows per table (HBM) or staging capacity (staged)
     void *out;           // float [n][512] or bf16 [n][512]
-    HashParams hp;       // IDX_HASH
+    HashParams hp;       // IDX_HASH, IDX_HASH_SHARD
+    int64_t shard_rows;  // IDX_HASH_SHARD: rows per table in this shard's tables
+    int32_t shard;       // IDX_HASH_SHARD: this shard, of n_shards
+    int32_t n_shards;
 };
 
 // 4 blocks of 256 threads per SM (at most 64 registers a thread; 3 blocks and
@@ -148,8 +156,13 @@ struct GatherParams {
 // carries eight E8M0 block scales (one per 32 codes) instead of one fp32.
 template <int kMode, bool kBf16Out, bool kMx>
 __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_constant__ GatherParams P) {
+    // The projection that consumes X may be launched as a programmatic
+    // dependent: its CTAs take SMs as this grid's last blocks drain and start
+    // on what does not depend on X.
+    allow_dependent_launch();
     __shared__ uint64_t s_seed[kTables];
-    if (kMode == IDX_HASH) {
+    constexpr bool kHashed = kMode == IDX_HASH || kMode == IDX_HASH_SHARD;
+    if (kHashed) {
         if (threadIdx.x < kTables) s_seed[threadIdx.x] = P.hp.seeds[threadIdx.x];
         if (blockIdx.x == 0 && threadIdx.x == 0 && P.hp.last_n == 0 &&
             __ldg(P.hp.offs + P.hp.n_seqs) - __ldg(P.hp.offs) != P.hp.n_query)
@@ -169,7 +182,7 @@ __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_c
     if (lane < kTablesPerModule) {
         const int j = kTablesPerModule * m + lane;
         int64_t r;
-        if (kMode == IDX_HASH) {
+        if (kHashed) {
             int64_t start, p;
             bool bad = !query_position(P.hp, t, start, p);
             r = bad ? -1 : hash_one(P.hp, s_seed[j], j, start, p, bad);
@@ -180,8 +193,15 @@ __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_c
             r = (int64_t)__ldg(static_cast<const int32_t *>(P.idx) + t * kTables + j);
         }
         ok = (r >= 0 && r < P.R);
-        if (!ok) raise_error(ENGRAM_ERANGE);
-        const int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
+        // a staged query with no slot (kSlotNone: the dedup overflowed or its
+        // index was out of range, both flagged there) contributes nothing
+        if (!ok && !(kMode == IDX_STAGED_I32 && r == kSlotNone)) raise_error(ENGRAM_ERANGE);
+        int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
+        if (kMode == IDX_HASH_SHARD && ok) {  // another shard's row adds nothing here
+            const int64_t k = r / P.n_shards;
+            ok = (r - k * P.n_shards) == P.shard;
+            flat = (int64_t)j * P.shard_rows + k;
+        }
         if (ok) {
             off = flat * P.row_stride;
             if (!kMx)
@@ -487,20 +507,23 @@ __global__ void __launch_bounds__(kScanThreads) dedup_emit_kernel(const uint32_t
     }
 }
 
+// Slot of each (query, table); kSlotNone for a row index out of range, and
+// for every query when the distinct rows overflowed the capacity (then nothing
+// is staged and the staged gather reads no row at all).
 __global__ void __launch_bounds__(256) dedup_remap_kernel(const int64_t *__restrict__ idx, int64_t n, int64_t R,
                                                           int64_t W, const uint32_t *__restrict__ bitmap,
                                                           const uint32_t *__restrict__ word_prefix,
-                                                          int64_t capacity, int32_t *__restrict__ idx_staged) {
+                                                          const int64_t *__restrict__ n_unique, int64_t capacity,
+                                                          int32_t *__restrict__ idx_staged) {
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n * kTables) return;
     const int j = (int)(g % kTables);
     const int64_t r = __ldg(idx + g);
-    int32_t slot = 0;
-    if (r >= 0 && r < R) {
+    int32_t slot = kSlotNone;
+    if (r >= 0 && r < R && *n_unique <= capacity) {
         const int64_t w = (int64_t)j * W + (r >> 5);
         const uint32_t below = __ldg(bitmap + w) & ((1u << (r & 31)) - 1u);
-        const int64_t s = (int64_t)__ldg(word_prefix + w) + __popc(below);
-        slot = s < capacity ? (int32_t)s : 0;
+        slot = (int32_t)((int64_t)__ldg(word_prefix + w) + __popc(below));
     }
     idx_staged[g] = slot;
 }
@@ -517,7 +540,8 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
                                                     const int64_t *__restrict__ unique,
                                                     const int64_t *__restrict__ n_unique, int64_t capacity,
                                                     uint8_t *__restrict__ staged, float *__restrict__ staged_scales) {
-    const int64_t U = min(*n_unique, capacity);
+    const int64_t U = *n_unique;
+    if (U > capacity) return;  // overflowed: the dedup flagged it and left no query pointing at a slot
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, c16 = lane & 15;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -649,7 +673,7 @@ static void fill_hash_params(HashParams &a, const engram_config *cfg, const int3
 // mx: rows carry eight E8M0 block scales at byte 256 (scales unused).
 engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const float *scales, int64_t stride,
                             bool mx, const void *idx, const HashParams *hp, int64_t n_query, int64_t R, void *out,
-                            cudaStream_t st) {
+                            cudaStream_t st, int64_t shard_rows = 0, int32_t shard = 0, int32_t n_shards = 1) {
     GatherParams P;
     memset(&P, 0, sizeof(P));
     P.rows = rows;
@@ -669,7 +693,12 @@ engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const 
         else                                                         \
             gather_kernel<M, B, false><<<blocks, 256, 0, st>>>(P);   \
     } while (0)
-    if (mode == IDX_I64) {
+    if (mode == IDX_HASH_SHARD) {  // fp32 partial sums only
+        P.shard_rows = shard_rows;
+        P.shard = shard;
+        P.n_shards = n_shards;
+        ENGRAM_GATHER(IDX_HASH_SHARD, false);
+    } else if (mode == IDX_I64) {
         if (bf16_out) ENGRAM_GATHER(IDX_I64, true); else ENGRAM_GATHER(IDX_I64, false);
     } else if (mode == IDX_STAGED_I32) {
         if (bf16_out) ENGRAM_GATHER(IDX_STAGED_I32, true); else ENGRAM_GATHER(IDX_STAGED_I32, false);
@@ -719,7 +748,7 @@ engram_status dedup_launch(const engram_config *cfg, const int64_t *idx, int64_t
     dedup_emit_kernel<<<(unsigned)L.n_blocks, kScanThreads, 0, st>>>(bitmap, L.n_words, L.W, cfg->rows, blocks,
                                                                       prefix, unique, capacity);
     if (n > 0)
-        dedup_remap_kernel<<<gb, 256, 0, st>>>(idx, n_query, cfg->rows, L.W, bitmap, prefix, capacity,
+        dedup_remap_kernel<<<gb, 256, 0, st>>>(idx, n_query, cfg->rows, L.W, bitmap, prefix, n_unique, capacity,
                                                idx_staged);
     return launch_status();
 }
@@ -805,11 +834,14 @@ enum FuseKind { FUSE_F32_MEM = 0, FUSE_BF16_X_GATE_WARPS = 2, FUSE_LAYER = 3 };
 // Persistent cluster launch: as many clusters of `groups` CTAs as fit at once
 // (cached per device and cluster size in *max_clusters), each striding over
 // the tiles.  attr_done / max_clusters belong to one kernel instantiation.
+// pdl: launch as a programmatic dependent of the previous kernel in the
+// stream (only after a gather kernel, which writes X and nothing the
+// projection reads before its grid_dependency_wait).
 template <typename Kern, typename... Args>
 static engram_status launch_persistent(Kern kern, int threads, int smem, int groups, int64_t m_tiles,
                                        std::atomic<bool> *attr_done,
                                        std::atomic<int> (*max_clusters)[fuse::MAX_GROUPS + 1], cudaStream_t st,
-                                       const Args &...args) {
+                                       bool pdl, const Args &...args) {
     int dev = 0;
     cudaGetDevice(&dev);
     const bool cache = dev >= 0 && dev < 64;
@@ -819,11 +851,13 @@ static engram_status launch_persistent(Kern kern, int threads, int smem, int gro
         if (cache) attr_done[dev].store(true, std::memory_order_relaxed);
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = groups;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -842,6 +876,7 @@ static engram_status launch_persistent(Kern kern, int threads, int smem, int gro
     }
     const int64_t clusters = std::min<int64_t>(m_tiles, mc);
     cfg.gridDim = dim3((unsigned)(clusters * groups));
+    if (pdl) cfg.numAttrs = 2;
     const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, args...);
     if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(fuse)");
     return launch_status();
@@ -859,7 +894,7 @@ static auto fuse_kernel_for() {
 
 template <int KIND, int CPG>
 static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hmap,
-                                   const fuse::Params &p, cudaStream_t st) {
+                                   const fuse::Params &p, cudaStream_t st, bool pdl) {
     constexpr bool k2 = KIND == FUSE_BF16_X_GATE_WARPS || KIND == FUSE_LAYER;
     constexpr int kThreads = k2 ? fuse2::NUM_THREADS : fuse::NUM_THREADS;
     constexpr int kSmem = k2 ? fuse2::SMEM_BYTES : fuse::SMEM_BYTES;
@@ -867,32 +902,32 @@ static engram_status fuse_launch_t(const CUtensorMap &wmap, const CUtensorMap &x
     static std::atomic<int> max_clusters[64][fuse::MAX_GROUPS + 1] = {};
     if constexpr (k2)
         return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
-                                 max_clusters, st, wmap, xmap, hmap, p);
+                                 max_clusters, st, pdl, wmap, xmap, hmap, p);
     else
         return launch_persistent(fuse_kernel_for<KIND, CPG>(), kThreads, kSmem, p.groups, p.m_tiles, attr_done,
-                                 max_clusters, st, wmap, xmap, p);
+                                 max_clusters, st, pdl, wmap, xmap, p);
 }
 
 template <int KIND>
 static engram_status fuse_dispatch(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hmap,
-                                   const fuse::Params &p, cudaStream_t st) {
+                                   const fuse::Params &p, cudaStream_t st, bool pdl = false) {
     switch (p.cpg) {
-        case 1: return fuse_launch_t<KIND, 1>(wmap, xmap, hmap, p, st);
-        case 2: return fuse_launch_t<KIND, 2>(wmap, xmap, hmap, p, st);
-        case 4: return fuse_launch_t<KIND, 4>(wmap, xmap, hmap, p, st);
-        case 8: return fuse_launch_t<KIND, 8>(wmap, xmap, hmap, p, st);
-        case 16: return fuse_launch_t<KIND, 16>(wmap, xmap, hmap, p, st);
+        case 1: return fuse_launch_t<KIND, 1>(wmap, xmap, hmap, p, st, pdl);
+        case 2: return fuse_launch_t<KIND, 2>(wmap, xmap, hmap, p, st, pdl);
+        case 4: return fuse_launch_t<KIND, 4>(wmap, xmap, hmap, p, st, pdl);
+        case 8: return fuse_launch_t<KIND, 8>(wmap, xmap, hmap, p, st, pdl);
+        case 16: return fuse_launch_t<KIND, 16>(wmap, xmap, hmap, p, st, pdl);
     }
     return ENGRAM_EINVAL;
 }
 
 template <int CPG>
 static engram_status fuse3_launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const CUtensorMap &hl,
-                                    const CUtensorMap &hs, const fuse::Params &p, cudaStream_t st) {
+                                    const CUtensorMap &hs, const fuse::Params &p, cudaStream_t st, bool pdl) {
     static std::atomic<bool> attr_done[64] = {};
     static std::atomic<int> max_clusters[64][fuse::MAX_GROUPS + 1] = {};
     return launch_persistent(fuse3::fuse3_kernel<CPG>, fuse3::NUM_THREADS, fuse3::smem_bytes<CPG>(), p.groups,
-                             p.m_tiles, attr_done, max_clusters, st, wmap, xmap, hl, hs, p);
+                             p.m_tiles, attr_done, max_clusters, st, pdl, wmap, xmap, hl, hs, p);
 }
 
 // Few tiles (under one per two SMs): the h-resident kernel, with d split into
@@ -909,8 +944,11 @@ static int pick_cpg_h_resident(int64_t m_tiles, int n_chunks) {
 // (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
 // split_tiles > 0: choose the kernel and the split of d as for a batch of
 // split_tiles tiles (a chunk of a larger batch then gives that batch's bits).
+// pdl (bf16 X only): launch as a programmatic dependent of the gather kernel
+// that was just enqueued on `st` and writes X.
 engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint16_t *x_bf16, const uint16_t *W,
-                          const uint16_t *g, uint16_t *h, int64_t n_query, cudaStream_t st, int64_t split_tiles = 0) {
+                          const uint16_t *g, uint16_t *h, int64_t n_query, cudaStream_t st, int64_t split_tiles = 0,
+                          bool pdl = false) {
     const int d = cfg->d_model;
     const int n_chunks = d / fuse::BN;
     fuse::Params p;
@@ -941,14 +979,15 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
             CUtensorMap hp;
             if (!bf16_map_2d(&hp, h, (uint64_t)d, (uint64_t)n_query, 64, 32))
                 return cuda_fail(cudaErrorInvalidValue, "h piece map");
-            return fuse_dispatch<FUSE_BF16_X_GATE_WARPS>(wmap, xmap, hp, p, st);
+            return fuse_dispatch<FUSE_BF16_X_GATE_WARPS>(wmap, xmap, hp, p, st, pdl);
         }
         {
             CUtensorMap hl, hs;  // h slice boxes: 64 columns x 128 tokens (loads) / x 32 tokens (stores)
             if (!bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, 64, fuse::BM) ||
                 !bf16_map_2d(&hs, h, (uint64_t)d, (uint64_t)n_query, 64, 32))
                 return cuda_fail(cudaErrorInvalidValue, "h tensor map");
-            return cpg3 == 1 ? fuse3_launch_t<1>(wmap, xmap, hl, hs, p, st) : fuse3_launch_t<2>(wmap, xmap, hl, hs, p, st);
+            return cpg3 == 1 ? fuse3_launch_t<1>(wmap, xmap, hl, hs, p, st, pdl)
+                             : fuse3_launch_t<2>(wmap, xmap, hl, hs, p, st, pdl);
         }
     }
     return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, xmap, p, st);
@@ -1149,7 +1188,7 @@ extern "C" engram_status engram_forward(const engram_config *cfg, const int32_t 
     engram_status s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), nullptr, &hp,
                                     n_query, cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
-    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st, 0, /*pdl=*/true);
 }
 
 extern "C" engram_status engram_gather_x(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
@@ -1166,6 +1205,31 @@ extern "C" engram_status engram_gather_x(const engram_config *cfg, const int32_t
     fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
     return gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), nullptr, &hp, n_query,
                          cfg->rows, X, (cudaStream_t)stream);
+}
+
+extern "C" int64_t engram_shard_rows(const engram_config *cfg, int32_t n_shards) {
+    if (check_config(cfg) != ENGRAM_OK || n_shards < 1) return 0;
+    return (cfg->rows + n_shards - 1) / n_shards;
+}
+
+extern "C" engram_status engram_gather_reduce_shard(const engram_config *cfg, int32_t shard, int32_t n_shards,
+                                                    const int32_t *tokens, const int64_t *seq_offsets, int64_t n_seqs,
+                                                    int32_t last_n, int64_t n_query, const uint8_t *tables_shard,
+                                                    const float *scales_shard, float *mem, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
+    if (n_shards < 1 || shard < 0 || shard >= n_shards) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !tables_shard || !scales_ok(cfg, scales_shard) || !mem)
+        return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (!aligned(tables_shard, 16) || !aligned(mem, 16) || !aligned(tokens, 4) || !aligned(seq_offsets, 8))
+        return ENGRAM_EINVAL;
+    if (n_query > (INT64_C(1) << 40)) return ENGRAM_EINVAL;
+    HashParams hp;
+    fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
+    return gather_launch(IDX_HASH_SHARD, false, tables_shard, scales_arg(cfg, scales_shard), row_stride(cfg), mx(cfg),
+                         nullptr, &hp, n_query, cfg->rows, mem, (cudaStream_t)stream,
+                         engram_shard_rows(cfg, n_shards), shard, n_shards);
 }
 
 extern "C" engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const uint16_t *W_out,
@@ -1510,11 +1574,12 @@ extern "C" engram_status engram_forward_no_workspace(const engram_config *cfg, c
                                                      void *stream) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
     if (n_query == 0) return ENGRAM_OK;
-    if (n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY) return ENGRAM_ENOMEM;  // past the built-in scratch
     if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales_ok(cfg, scales)) return ENGRAM_EINVAL;
     if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
     if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
     if (!aligned(tables, 16) || !aligned(tokens, 4) || !aligned(seq_offsets, 8)) return ENGRAM_EINVAL;
+    // as engram_forward: a size the scratch cannot hold only after every argument check
+    if (n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY) return ENGRAM_ENOMEM;
     uint16_t *X = nullptr;
     engram_status s = no_workspace_scratch(&X);
     if (s != ENGRAM_OK) return s;

@@ -153,6 +153,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool issued[NSTAGE] = {};
             uint32_t issued_parity[NSTAGE] = {};
+            // X is the previous kernel's output; h and g, which the gate warps
+            // read meanwhile, are not written by it (launched as a programmatic
+            // dependent of the gather only).
+            grid_dependency_wait();
             for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl) {
                 for (int c = c0; c < c0 + CPG && !*abort; ++c) {
                     for (int ks = 0; ks < KB; ++ks) {

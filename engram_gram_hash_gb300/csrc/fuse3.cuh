@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool issued[NSTAGE] = {};
             uint32_t issued_parity[NSTAGE] = {};
+            grid_dependency_wait();  // X comes from the previous kernel (h does not)
             for (int64_t mt = cl; mt < p.m_tiles && !*abort; mt += n_cl) {
                 for (int c = c0; c < c0 + CPG && !*abort; ++c) {
                     for (int ks = 0; ks < KSTAGES; ++ks) {

@@ -168,6 +168,29 @@ engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const u
                             uint16_t *h, int64_t n_query, void *stream);
 
 /*
+ * Row-sharded tables ("Engram: the table that is never multiplied": SGLang
+ * splits the tables by row across tensor-parallel GPUs, at the cost of one
+ * all-reduce per Engram layer).  Row r of every table belongs to shard
+ * r mod n_shards and is stored there as local row r / n_shards, so each
+ * shard holds engram_shard_rows(cfg, n_shards) = ceil(R / n_shards) rows per
+ * table (the last one unused on some shards).
+ * engram_gather_reduce_shard: steps 1-3 for every query token, reading only
+ *   this shard's rows (hashed in registers as in engram_gather_x):
+ *   mem[t][256m + c] = sum over module m's tables j whose row idx[t][j] this
+ *   shard owns of scale * e4m3 value, fp32, other rows adding nothing.
+ *   tables_shard [48][ceil(R/n)][256 or 272] and scales_shard [48][ceil(R/n)]
+ *   in the layouts of engram_gather_reduce; mem fp32 [n_query][512] output.
+ *   The sum over all shards of their mem (the one exchange: an all-reduce,
+ *   or a reduce-scatter over tokens) is the whole mem up to fp32 summation
+ *   order; engram_fuse then applies steps 4-5.  shard in [0, n_shards).
+ */
+int64_t engram_shard_rows(const engram_config *cfg, int32_t n_shards);
+engram_status engram_gather_reduce_shard(const engram_config *cfg, int32_t shard, int32_t n_shards,
+                                         const int32_t *tokens, const int64_t *seq_offsets, int64_t n_seqs,
+                                         int32_t last_n, int64_t n_query, const uint8_t *tables_shard,
+                                         const float *scales_shard, float *mem, void *stream);
+
+/*
  * engram_forward without a workspace argument.  The sources have no
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory -- code running inside a host engine or framework that owns
@@ -180,11 +203,14 @@ engram_status engram_fuse_x(const engram_config *cfg, const uint16_t *X, const u
  *   - Allocates nothing and calls no allocating CUDA or library routine.
  *   - Every GPU that loads libengram.so holds that array until the process
  *     exits.
- *   - n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY returns ENGRAM_ENOMEM and
- *     enqueues nothing; other arguments are checked as for engram_forward.
+ *   - Arguments are checked as for engram_forward (ENGRAM_EINVAL first);
+ *     then n_query > ENGRAM_NO_WORKSPACE_MAX_QUERY returns ENGRAM_ENOMEM.
+ *     Either way nothing is enqueued.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
- *     any stream capture on the device.
+ *     any stream capture on the device.  The address is kept for the life of
+ *     the process: do not call this entry point on a device after
+ *     cudaDeviceReset() on it (the array may then live elsewhere).
  *   - Every call shares the one array: two calls that overlap on the GPU
  *     (different streams, or different host threads on one device) race on
  *     it and give undefined results.  Calls in one stream are ordered and
@@ -207,9 +233,11 @@ engram_status engram_forward_no_workspace(const engram_config *cfg, const int32_
  *   workspace   >= engram_dedup_workspace_bytes(cfg) bytes, 256-byte aligned
  *   unique      int64 [capacity] output: flat row j*R + row of slot u
  *   idx_staged  int32 [n_query][48] output: slot of (t, j)
- *   n_unique    int64 [1] output (device): number of distinct rows U; if
- *               U > capacity only the first `capacity` slots are written, the
- *               other queries point at slot 0 and ENGRAM_ECAPACITY is set.
+ *   n_unique    int64 [1] output (device): number of distinct rows U.
+ * If U > capacity, ENGRAM_ECAPACITY is set on the device, every idx_staged
+ * entry is -1 (no slot: an index out of range also gets -1, with
+ * ENGRAM_ERANGE), engram_stage then copies nothing and the staged gather
+ * reads no row (mem = 0), so engram_forward_host leaves h as it was.
  */
 size_t engram_dedup_workspace_bytes(const engram_config *cfg);
 engram_status engram_dedup(const engram_config *cfg, const int64_t *idx, int64_t n_query, void *workspace,
@@ -217,8 +245,9 @@ engram_status engram_dedup(const engram_config *cfg, const int64_t *idx, int64_t
                            int64_t *n_unique, void *stream);
 
 /*
- * engram_stage: copy the U = min(*n_unique, capacity) unique rows and their
- * scales from host tables into device staging buffers.
+ * engram_stage: copy the U = *n_unique unique rows and their scales from
+ * host tables into device staging buffers; if U > capacity it copies nothing
+ * (the dedup has already set ENGRAM_ECAPACITY).
  *   host_tables e4m3 [48][R][256] (or [48][R][272] records) in pinned host
  *               memory (16-byte aligned)
  *   host_scales fp32 [48][R] in pinned host memory (ENGRAM_ROWS_SEPARATE only)
@@ -237,7 +266,9 @@ engram_status engram_stage(const engram_config *cfg, const uint8_t *host_tables,
  * engram_gather_reduce, so its output is bit-identical to the HBM path on
  * the same inputs (SGLang's host-table mode is documented as bitwise
  * identical, "Engram: the table that is never multiplied").  Staging
- * layouts as in engram_stage.
+ * layouts as in engram_stage.  An idx_staged entry of -1 names no row and
+ * adds nothing (the dedup's overflow or range error is already flagged);
+ * any other entry outside [0, capacity) sets ENGRAM_ERANGE.
  */
 engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_t *staged_rows,
                                           const float *staged_scales, const int32_t *idx_staged,
@@ -258,28 +289,6 @@ engram_status engram_forward_host(const engram_config *cfg, const int32_t *token
                                   int64_t *n_unique, void *stream, void *side_stream, void *ev_dedup,
                                   void *ev_staged);
 
-/*
- * The host-table path pipelined over chunks of `chunk` query tokens (the
- * pages' background prefetch of host rows on a side stream, "Engram: the table
- * that is never multiplied", applied chunk by chunk).  All queries are hashed
- * first; then, for chunk k, the unique rows are found on `stream` and staged
- * on `side_stream` into one of two staging sets (k mod 2), and the staged
- * gather of chunk k runs on `stream` while chunk k+1 is being deduplicated and
- * staged; one projection over the whole batch follows.  h equals
- * engram_forward's on the same tables bit for bit.  Rows used by several
- * chunks cross the host link once per chunk.
- *   chunk       query tokens per chunk (>= 1; a multiple of 128 keeps whole
- *               tiles per chunk)
- *   capacity    staging rows per set; at least the unique rows of any chunk
- *               (chunk * 48 always suffices); more raise ENGRAM_ECAPACITY
- *   n_unique    int64 [ceil(n_query / chunk)] (device): unique rows per chunk
- *   events      6 caller-created events (cudaEventDisableTiming is fine):
- *               dedup done x2, staged x2, staging set consumed x2
- * workspace >= engram_forward_host_pipelined_workspace_bytes(cfg, n_query,
- * chunk, capacity); host tables and scales as in engram_forward_host.
- * Argument errors return synchronously; device-side range and capacity errors
- * set the sticky error word.
- */
 /*
  * The per-layer form of the Engram read (rohitghumare.com
  * "guides/deepseek-v4-1-flash": section "The architecture", layers 1 and 14
@@ -331,6 +340,28 @@ engram_status engram_layer_forward(const engram_config *cfg, int32_t module, con
 engram_status engram_host_alloc(size_t bytes, void **ptr);
 engram_status engram_host_free(void *ptr);
 
+/*
+ * The host-table path pipelined over chunks of `chunk` query tokens (the
+ * pages' background prefetch of host rows on a side stream, "Engram: the table
+ * that is never multiplied", applied chunk by chunk).  All queries are hashed
+ * first; then, for chunk k, the unique rows are found on `stream` and staged
+ * on `side_stream` into one of two staging sets (k mod 2), and the staged
+ * gather of chunk k runs on `stream` while chunk k+1 is being deduplicated and
+ * staged; one projection over the whole batch follows.  h equals
+ * engram_forward's on the same tables bit for bit.  Rows used by several
+ * chunks cross the host link once per chunk.
+ *   chunk       query tokens per chunk (>= 1; a multiple of 128 keeps whole
+ *               tiles per chunk)
+ *   capacity    staging rows per set; at least the unique rows of any chunk
+ *               (chunk * 48 always suffices); more raise ENGRAM_ECAPACITY
+ *   n_unique    int64 [ceil(n_query / chunk)] (device): unique rows per chunk
+ *   events      6 caller-created events (cudaEventDisableTiming is fine):
+ *               dedup done x2, staged x2, staging set consumed x2
+ * workspace >= engram_forward_host_pipelined_workspace_bytes(cfg, n_query,
+ * chunk, capacity); host tables and scales as in engram_forward_host.
+ * Argument errors return synchronously; device-side range and capacity errors
+ * set the sticky error word.
+ */
 size_t engram_forward_host_pipelined_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t chunk,
                                                      int64_t capacity);
 engram_status engram_forward_host_pipelined(const engram_config *cfg, const int32_t *tokens,

