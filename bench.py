@@ -855,7 +855,10 @@ def run_reference(args, rank, world):
 
 def run_probe(args):
     """Ceilings for the gather: random 256-byte rows over a large buffer, with
-    and without one 4-byte scale per row from a second array."""
+    and without one 4-byte scale per row from a second array; and the host
+    link measured two ways: random 256-byte rows read by the kernel from
+    pinned host memory over unified addressing (zero-copy), and a pinned
+    host-to-device cudaMemcpyAsync."""
     import ctypes
 
     import torch
@@ -887,7 +890,68 @@ def run_probe(args):
         useful = n_warps * 24 * (256 + (4 if sc is not None else 0))
         out[name] = {"ms": round(ms, 4), "useful_GBps": round(useful / ms / 1e6, 1),
                      "frac_of_copy_peak": round(useful / ms / 1e6 / measured_peaks()["hbm_gbs"], 3)}
+    # the scale read's cache operator (scattered 4-byte reads: the DRAM bytes each costs)
+    lib.probe_random_rows_flavor.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    names = ["ld.global.nc", "ld.global.cg", "ld.global.nc.L1::no_allocate", "ld.global.L1::no_allocate"]
+    out["scale_load"] = {}
+    for fl, nm in enumerate(names):
+        for k in range(2):
+            lib.probe_random_rows_flavor(ctypes.c_void_p(rows.data_ptr()), ctypes.c_void_p(scales.data_ptr()), n_rows,
+                                         n_warps, k, ctypes.c_void_p(sink.data_ptr()), fl, st)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for k in range(10):
+            lib.probe_random_rows_flavor(ctypes.c_void_p(rows.data_ptr()), ctypes.c_void_p(scales.data_ptr()), n_rows,
+                                         n_warps, 300 + k, ctypes.c_void_p(sink.data_ptr()), fl, st)
+        b.record()
+        torch.cuda.synchronize()
+        out["scale_load"][nm] = {"ms": round(a.elapsed_time(b) / 10, 4)}
+    del rows, scales
+    if args.probe_host_gb > 0:
+        out["host_link"] = probe_host_link(lib, args.probe_host_gb, sink, st)
     return out
+
+
+def probe_host_link(lib, host_gb, sink, st):
+    """The host-link denominator two ways: zero-copy random 256-byte rows
+    from pinned host memory (the staging kernel's access pattern), and a
+    pinned host-to-device copy of 2 GiB."""
+    import ctypes
+
+    import torch
+
+    n_rows = 1 << ((host_gb << 30) // 256).bit_length() - 1
+    host = torch.empty(n_rows * 256, dtype=torch.uint8, pin_memory=True)
+    host[::4096].fill_(1)  # touch every page
+    n_warps = 16384  # 393,216 rows = 100 MB per launch
+    res = {"buffer_GB": round(n_rows * 256 / 2**30, 1), "rows_per_launch": n_warps * 24}
+    lib.probe_random_host_rows.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                                           ctypes.c_void_p, ctypes.c_void_p]
+    for k in range(2):
+        lib.probe_random_host_rows(ctypes.c_void_p(host.data_ptr()), n_rows, n_warps, k,
+                                   ctypes.c_void_p(sink.data_ptr()), st)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    a.record()
+    for k in range(reps):
+        lib.probe_random_host_rows(ctypes.c_void_p(host.data_ptr()), n_rows, n_warps, 200 + k,
+                                   ctypes.c_void_p(sink.data_ptr()), st)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    res["zero_copy_random_rows"] = {"ms": round(ms, 3), "GBps": round(n_warps * 24 * 256 / ms / 1e6, 1)}
+    src = host[: 1 << 31]
+    dst = torch.empty(1 << 31, dtype=torch.uint8, device="cuda")
+    dst.copy_(src, non_blocking=True)
+    a.record()
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    res["pinned_h2d_copy"] = {"GBps": round(3 * (1 << 31) / (a.elapsed_time(b) * 1e-3) / 1e9, 1)}
+    res["denominator_GBps"] = max(res["zero_copy_random_rows"]["GBps"], res["pinned_h2d_copy"]["GBps"])
+    return res
 
 
 def launch_ranks(n, argv=None):
@@ -930,6 +994,7 @@ def main():
                     help="chunk sizes for the pipelined host-table path (host workload)")
     ap.add_argument("--probe", action="store_true", help="print the random-row bandwidth ceilings and exit")
     ap.add_argument("--probe-gb", type=int, default=32)
+    ap.add_argument("--probe-host-gb", type=int, default=16, help="pinned host buffer for the host-link probe (0: skip)")
     ap.add_argument("--rows", type=int, default=0, help="override R (reduced case for profiling)")
     ap.add_argument("--tokens", type=int, default=0, help="override tokens per sequence (reduced case)")
     args = ap.parse_args()

@@ -25,6 +25,7 @@
 #include "fuse2.cuh"
 #include "fuse3.cuh"
 #include "layer.cuh"
+#include "narrow.cuh"
 
 namespace engram {
 
@@ -137,6 +138,57 @@ constexpr int32_t kSlotNone = -1;  // idx_staged entry that names no staged row
 
 enum ScaleMode { SCALE_ARRAY = 0, SCALE_IN_ROW = 1, SCALE_MX = 2 };
 
+// Token gates computed beside the gather for the d-split projection
+// (narrow.cuh), in the projection kernels' reduction order: d in `groups`
+// slices of cpg 256-column chunks; per slice, lane l sums its 16-byte pieces
+// l, l+32, ... (fmaf in column order), a butterfly adds the lanes, and the
+// slices' sums are added in slice order; then
+// gate = sigmoid(rsqrt(sum h^2 / d + eps) * <h,g> / sqrt(d)).
+struct GateParams {
+    const uint16_t *h;  // [n_query][d] bf16
+    const uint16_t *g;  // [d] bf16
+    float *gate;        // [n_query] out
+    int64_t gather_blocks;
+    int32_t d, groups, cpg;
+    float eps, inv_sqrt_d;
+};
+
+__device__ __forceinline__ void gate_pass(const GateParams &G, int64_t n_query, int64_t warp_id, int lane) {
+    const int64_t t = warp_id;
+    if (t >= n_query) return;
+    const uint16_t *hrow = G.h + t * G.d;
+    float ssum = 0.f, dsum = 0.f;
+    for (int r = 0; r < G.groups; ++r) {
+        const int col0 = r * G.cpg * fuse::BN;
+        float s = 0.f, d = 0.f;
+        for (int k = 0; k < G.cpg; ++k) {
+            const int ci = lane + 32 * k;  // 16-byte piece of the slice
+            const uint4 hv = __ldg(reinterpret_cast<const uint4 *>(hrow + col0) + ci);
+            const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(G.g + col0) + ci);
+            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a0 = bf16_lo(hw[e]), a1 = bf16_hi(hw[e]);
+                s = fmaf(a0, a0, s);
+                s = fmaf(a1, a1, s);
+                d = fmaf(a0, bf16_lo(gw[e]), d);
+                d = fmaf(a1, bf16_hi(gw[e]), d);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+            d += __shfl_xor_sync(0xffffffffu, d, o);
+        }
+        ssum += s;
+        dsum += d;
+    }
+    const float rinv = rsqrtf(ssum / (float)G.d + G.eps);
+    const float gate = 1.f / (1.f + __expf(-(rinv * dsum * G.inv_sqrt_d)));
+    if (lane == 0) G.gate[t] = gate;
+}
+
 struct GatherParams {
     const uint8_t *rows;
     const float *scales;     // fp32 [rows], or nullptr when each row carries its scale bytes at byte 256
@@ -149,17 +201,25 @@ struct GatherParams {
     int64_t shard_rows;  // IDX_HASH_SHARD: rows per table in this shard's tables
     int32_t shard;       // IDX_HASH_SHARD: this shard, of n_shards
     int32_t n_shards;
+    GateParams gp;       // kGate: blocks from gather_blocks on compute the token gates
 };
 
 // 4 blocks of 256 threads per SM (at most 64 registers a thread; 3 blocks and
 // 80 registers for kMx, which also holds twelve scale bytes a lane).  kMx: each row
 // carries eight E8M0 block scales (one per 32 codes) instead of one fp32.
-template <int kMode, bool kBf16Out, bool kMx>
+template <int kMode, bool kBf16Out, bool kMx, bool kGate = false>
 __global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_constant__ GatherParams P) {
     // The projection that consumes X may be launched as a programmatic
     // dependent: its CTAs take SMs as this grid's last blocks drain and start
     // on what does not depend on X.
     allow_dependent_launch();
+    if constexpr (kGate) {  // the blocks past the gather's compute token gates
+        if ((int64_t)blockIdx.x >= P.gp.gather_blocks) {
+            gate_pass(P.gp, P.n_query, ((int64_t)(blockIdx.x - P.gp.gather_blocks) * blockDim.x + threadIdx.x) >> 5,
+                      threadIdx.x & 31);
+            return;
+        }
+    }
     __shared__ uint64_t s_seed[kTables];
     constexpr bool kHashed = kMode == IDX_HASH || kMode == IDX_HASH_SHARD;
     if (kHashed) {
@@ -785,9 +845,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensormap_encoder() {
 }
 
 // 2-D bf16 tensor [outer][inner] (inner contiguous), box [box_outer][box_inner],
-// 128-byte swizzle: a box row of 64 bf16 is one swizzle span.
+// 128-byte swizzle (a box row of 64 bf16 is one swizzle span) or 64-byte
+// swizzle (box rows of 32 bf16).
 static bool bf16_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                        uint32_t box_outer) {
+                        uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = tensormap_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -795,7 +856,7 @@ static bool bf16_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -940,6 +1001,8 @@ static int pick_cpg_h_resident(int64_t m_tiles, int n_chunks) {
     return 0;
 }
 
+static bool fuse_split(int64_t m_tiles, int n_chunks, int *groups, int *cpg);
+
 // y = X @ W_out and the gated residual update.  X comes either from fp32 mem
 // (converted in the kernel) or from a bf16 [n_query][512] tensor via TMA.
 // split_tiles > 0: choose the kernel and the split of d as for a batch of
@@ -961,15 +1024,13 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     // One split of d for both inputs (fp32 mem or bf16 X), so they agree bit for bit.
     const int64_t tiles_for_split = split_tiles > 0 ? split_tiles : p.m_tiles;
     const int cpg3 = pick_cpg_h_resident(tiles_for_split, n_chunks);
-    p.groups = cpg3 ? n_chunks / cpg3 : pick_groups(tiles_for_split, n_chunks);
-    if (p.groups == 0) return ENGRAM_EINVAL;
-    p.cpg = n_chunks / p.groups;
+    if (!fuse_split(tiles_for_split, n_chunks, &p.groups, &p.cpg)) return ENGRAM_EINVAL;
     p.eps = cfg->rms_eps;
     p.inv_sqrt_d = 1.0f / sqrtf((float)d);
-    if (p.cpg > 16) return ENGRAM_EINVAL;
     CUtensorMap wmap, xmap;
     memset(&xmap, 0, sizeof(xmap));
-    // W boxes: 64 columns x WBK K-rows (fuse.cuh) or x BK K-rows (fuse2.cuh, one ring stage)
+    // W boxes: 64 columns x WBK K-rows (fuse.cuh) or x BK K-rows (fuse2.cuh and
+    // fuse3.cuh, one ring stage)
     const uint32_t w_box_rows = x_bf16 ? fuse::BK : fuse::WBK;
     if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, 64, w_box_rows)) return cuda_fail(cudaErrorInvalidValue, "W tensor map");
     if (x_bf16) {
@@ -1060,7 +1121,96 @@ engram_status check_fuse_args(const engram_config *cfg, const void *W, const voi
 }
 
 // forward workspace: X [n][512] bf16
-static size_t forward_bytes(int64_t n) { return round_up((size_t)n * kMem * 2, 256); }
+// forward workspace: X [n][512] bf16 | gate [n] fp32 (the d-split projection's gates)
+static size_t forward_x_bytes(int64_t n) { return round_up((size_t)n * kMem * 2, 256); }
+static size_t forward_bytes(int64_t n) { return forward_x_bytes(n) + round_up((size_t)n * 4, 256); }
+
+// The d-split projection (narrow.cuh) when every (tile, 64-column slice) of
+// the batch gets an SM of its own: one wave, no cluster.
+static bool narrow_fits(int64_t m_tiles, int d) {
+    return d % narrow::BN == 0 && m_tiles * (d / narrow::BN) <= num_sms();
+}
+
+// The split of d that fuse_launch would choose for a batch of m_tiles tiles:
+// groups slices of cpg 256-column chunks (the token gates' reduction order).
+static bool fuse_split(int64_t m_tiles, int n_chunks, int *groups, int *cpg) {
+    const int cpg3 = pick_cpg_h_resident(m_tiles, n_chunks);
+    *groups = cpg3 ? n_chunks / cpg3 : pick_groups(m_tiles, n_chunks);
+    if (*groups == 0) return false;
+    *cpg = n_chunks / *groups;
+    return *cpg <= 16;
+}
+
+// Hash + gather -> bf16 X, plus one warp per query token computing its gate
+// in fuse_split's order (extra blocks of the same launch).
+static engram_status gather_gate_launch(const engram_config *cfg, const uint8_t *tables, const float *scales,
+                                        const HashParams &hp, int64_t n_query, uint16_t *X, const uint16_t *h,
+                                        const uint16_t *g, float *gate, int groups, int cpg, cudaStream_t st) {
+    GatherParams P;
+    memset(&P, 0, sizeof(P));
+    P.rows = tables;
+    P.scales = scales_arg(cfg, scales);
+    P.row_stride = row_stride(cfg);
+    P.n_query = n_query;
+    P.R = cfg->rows;
+    P.out = X;
+    P.hp = hp;
+    const int64_t gather_blocks = (n_query * 2 * 32 + 255) / 256;
+    const int64_t gate_blocks = (n_query * 32 + 255) / 256;
+    P.gp.h = h;
+    P.gp.g = g;
+    P.gp.gate = gate;
+    P.gp.gather_blocks = gather_blocks;
+    P.gp.d = cfg->d_model;
+    P.gp.groups = groups;
+    P.gp.cpg = cpg;
+    P.gp.eps = cfg->rms_eps;
+    P.gp.inv_sqrt_d = 1.0f / sqrtf((float)cfg->d_model);
+    const unsigned blocks = (unsigned)(gather_blocks + gate_blocks);
+    if (mx(cfg))
+        gather_kernel<IDX_HASH, true, true, true><<<blocks, 256, 0, st>>>(P);
+    else
+        gather_kernel<IDX_HASH, true, false, true><<<blocks, 256, 0, st>>>(P);
+    return launch_status();
+}
+
+// h = bf16(h + gate * X W_out) by the d-split kernel, launched as a
+// programmatic dependent of the gather_gate_launch just enqueued on `st`.
+static engram_status narrow_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W, const float *gate,
+                                   uint16_t *h, int64_t n_query, cudaStream_t st) {
+    const int d = cfg->d_model;
+    CUtensorMap wmap, xmap, hl, hs;
+    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, narrow::BN, narrow::BK) ||
+        !bf16_map_2d(&xmap, X, kMem, (uint64_t)n_query, narrow::BK, narrow::BM) ||
+        !bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, narrow::BM) ||
+        !bf16_map_2d(&hs, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, 32))
+        return cuda_fail(cudaErrorInvalidValue, "narrow projection tensor maps");
+    static std::atomic<bool> attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(narrow::narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, narrow::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(narrow smem)");
+        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
+    }
+    narrow::Params p;
+    p.gate = gate;
+    p.n_query = n_query;
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = dim3((unsigned)(d / narrow::BN), (unsigned)((n_query + narrow::BM - 1) / narrow::BM));
+    lc.blockDim = dim3(narrow::NUM_THREADS);
+    lc.dynamicSmemBytes = narrow::SMEM_BYTES;
+    lc.stream = st;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const cudaError_t le = cudaLaunchKernelEx(&lc, narrow::narrow_kernel, wmap, xmap, hl, hs, p);
+    if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(narrow)");
+    return launch_status();
+}
 
 }  // namespace engram
 
@@ -1185,6 +1335,16 @@ extern "C" engram_status engram_forward(const engram_config *cfg, const int32_t 
     uint16_t *X = static_cast<uint16_t *>(workspace);
     HashParams hp;
     fill_hash_params(hp, cfg, tokens, seq_offsets, n_seqs, last_n, n_query);
+    const int64_t m_tiles = (n_query + fuse::BM - 1) / fuse::BM;
+    int groups = 0, cpg = 0;
+    if (narrow_fits(m_tiles, cfg->d_model) && fuse_split(m_tiles, cfg->d_model / fuse::BN, &groups, &cpg)) {
+        // few tokens: gates beside the gather, then d split over one CTA per
+        // 64 columns (the same bits as the cluster kernels)
+        float *gate = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + forward_x_bytes(n_query));
+        engram_status s = gather_gate_launch(cfg, tables, scales, hp, n_query, X, h, g, gate, groups, cpg, st);
+        if (s != ENGRAM_OK) return s;
+        return narrow_launch(cfg, X, W_out, gate, h, n_query, st);
+    }
     engram_status s = gather_launch(IDX_HASH, true, tables, scales_arg(cfg, scales), row_stride(cfg), mx(cfg), nullptr, &hp,
                                     n_query, cfg->rows, X, st);
     if (s != ENGRAM_OK) return s;
