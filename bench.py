@@ -370,6 +370,120 @@ def time_host_pipelined(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, 
             "rows_staged_per_step": int(n_unique.sum().item()), "steps": steps}
 
 
+def time_host_cached(eg, c, cfg, tables, scales, W, g, h, dev, slots, steps):
+    """The host-table path on a stream of distinct token batches (one per
+    call), with and without the HBM cache of staged rows: ms per step, the
+    cache's hit rate and the rows that crossed the host link."""
+    import torch
+
+    from synth.configs import make_tokens
+
+    nq = cfg.tq
+    n_b = steps + 3
+    batches = []
+    for k in range(n_b):
+        tok, offs = make_tokens(cfg.with_(seed=cfg.seed * 1000 + 17 + k))
+        batches.append((torch.from_numpy(tok).to(dev), torch.from_numpy(offs).to(dev)))
+    cap = nq * 48
+    cache = eg.engram_host_cache_new(c, slots, cap, device=dev)
+    ws = torch.empty(eg.engram_forward_host_cached_workspace_bytes(c, nq, cap), dtype=torch.uint8, device=dev)
+    stats = torch.zeros((n_b, 4), dtype=torch.int64, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    ea, eb = torch.cuda.Event(), torch.cuda.Event()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(3):  # warm-up calls fill the cache
+        eg.engram_forward_host_cached(c, batches[k][0], batches[k][1], tables, scales, W, g, h, cache, slots, cap,
+                                      stamp=k + 1, n_query=nq, workspace=ws, stats=stats[k], side_stream=side,
+                                      ev_dedup=ea, ev_staged=eb)
+    torch.cuda.synchronize()
+    a.record()
+    for k in range(3, n_b):
+        eg.engram_forward_host_cached(c, batches[k][0], batches[k][1], tables, scales, W, g, h, cache, slots, cap,
+                                      stamp=k + 1, n_query=nq, workspace=ws, stats=stats[k], side_stream=side,
+                                      ev_dedup=ea, ev_staged=eb)
+    b.record()
+    torch.cuda.synchronize()
+    if eg.engram_last_error() != 0:
+        raise RuntimeError("device error in the cached host path")
+    ms_cached = a.elapsed_time(b) / steps
+    st = stats[3:].double().cpu().numpy()
+    fws = torch.empty(eg.engram_forward_host_workspace_bytes(c, nq, cap), dtype=torch.uint8, device=dev)
+    nu = torch.zeros(1, dtype=torch.int64, device=dev)
+    a.record()
+    for k in range(3, n_b):
+        eg.engram_forward_host(c, batches[k][0], batches[k][1], tables, scales, W, g, h, cap, n_query=nq,
+                               workspace=fws, n_unique=nu, side_stream=side, ev_dedup=ea, ev_staged=eb)
+    b.record()
+    torch.cuda.synchronize()
+    ms_plain = a.elapsed_time(b) / steps
+    return {"slots": slots, "steps": steps, "batches": "a new token batch every call",
+            "ms_per_step": round(ms_cached, 4), "tokens_per_s": round(nq / (ms_cached * 1e-3), 1),
+            "uncached_ms_per_step": round(ms_plain, 4),
+            "distinct_rows_per_step": round(float(st[:, 0].mean()), 1),
+            "hit_rate": round(float(st[:, 1].sum() / st[:, 0].sum()), 4),
+            "rows_over_link_per_step": round(float(st[:, 2].mean()), 1),
+            "overflow_rows_per_step": round(float(st[:, 3].mean()), 1),
+            "link_bytes_per_step": round(float(st[:, 2].mean()) * 260)}
+
+
+def time_workload(eg, name, dev, steps, warmup):
+    """engram_forward on another workload of the measurement plan, timed the
+    same way (CUDA events around `steps` calls after `warmup`): ms per step,
+    tokens/s and the fraction of the nominal-bytes roofline; decode-sized
+    batches also eager against CUDA-graph replay."""
+    import torch
+
+    from synth import device as sd
+    from synth.configs import CONFIGS, default_seeds, make_tokens
+
+    cfg = CONFIGS[name]
+    c = eg.make_config(cfg.V, cfg.R, cfg.d, default_seeds(), cfg.rms_eps)
+    tok, offs = make_tokens(cfg)
+    tokens, seq_offsets = torch.from_numpy(tok).to(dev), torch.from_numpy(offs).to(dev)
+    tables = torch.zeros((48, cfg.R, 256), dtype=torch.uint8, device=dev)
+    sd.fill_tables(tables, cfg.seed)
+    scales = torch.empty((48, cfg.R), dtype=torch.float32, device=dev)
+    sd.fill_scales(scales, cfg.seed)
+    W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=dev)
+    g = torch.empty(cfg.d, dtype=torch.bfloat16, device=dev)
+    h = torch.empty((cfg.tq, cfg.d), dtype=torch.bfloat16, device=dev)
+    sd.fill_w_out(W, cfg.seed)
+    sd.fill_g(g, cfg.seed)
+    sd.fill_h(h, cfg.seed)
+    nq = cfg.tq
+    ws = torch.empty(eg.engram_forward_workspace_bytes(c, nq), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        eg.engram_forward(c, tokens, seq_offsets, tables, scales, W, g, h, last_n=cfg.last_n, n_query=nq,
+                          workspace=ws)
+
+    for _ in range(warmup):
+        fwd()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fwd()
+    b.record()
+    torch.cuda.synchronize()
+    if eg.engram_last_error() != 0:
+        raise RuntimeError(f"device error in the {name} workload")
+    ms = a.elapsed_time(b) / steps
+    gbs = nominal_bytes_per_token(cfg.d) * nq / (ms * 1e-3) / 1e9
+    res = {"workload": name, "query_tokens": nq, "R": cfg.R, "steps": steps, "ms_per_step": round(ms, 4),
+           "tokens_per_s": round(nq / (ms * 1e-3), 1), "step_roofline_frac": round(gbs / measured_peaks()["hbm_gbs"], 4)}
+    if nq <= 4096:
+        res["cuda_graph"] = time_forward_graph(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
+                                               max(steps, 200))
+        w_out = 512 * cfg.d * 2
+        res["step_frac_with_W_out"] = round(
+            (nominal_bytes_per_token(cfg.d) * nq + w_out) / (res["cuda_graph"]["graph_us_per_step"] * 1e-6) / 1e9
+            / measured_peaks()["hbm_gbs"], 4)
+    del tables, scales, h, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -644,10 +758,17 @@ def run_ours(args, rank, world, local_rank):
         out["pipelined"] = [time_host_pipelined(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
                                                 ch, max(3, min(K, 20)))
                             for ch in args.host_chunks if 0 < ch < nq]
+        if args.host_cache_slots > 0 and args.layout != "mx":
+            out["cached"] = time_host_cached(eg, c, cfg, tables, scales, W, g, h, dev, args.host_cache_slots,
+                                             max(3, min(K, 20)))
     if not args.no_e2e and not layers and not sharded:
         out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not layers and not sharded:
         out["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    if world == 1 and args.also and not (args.rows or args.tokens or layers or sharded or host):
+        del tables, scales
+        torch.cuda.empty_cache()
+        out["also"] = [time_workload(eg, nm, dev, 20, 5) for nm in args.also.split(",") if nm and nm != args.workload]
     return out
 
 
@@ -992,6 +1113,10 @@ def main():
                     help="host tables in engram_host_alloc memory (huge pages) or torch pinned memory")
     ap.add_argument("--host-chunks", type=int, nargs="*", default=[32768],
                     help="chunk sizes for the pipelined host-table path (host workload)")
+    ap.add_argument("--also", default="prefill,decode",
+                    help="other workloads timed after the main line (engram_forward, 20 steps), comma-separated")
+    ap.add_argument("--host-cache-slots", type=int, default=1 << 24,
+                    help="rows of the HBM cache of staged rows timed beside the host-table path (0: skip)")
     ap.add_argument("--probe", action="store_true", help="print the random-row bandwidth ceilings and exit")
     ap.add_argument("--probe-gb", type=int, default=32)
     ap.add_argument("--probe-host-gb", type=int, default=16, help="pinned host buffer for the host-link probe (0: skip)")

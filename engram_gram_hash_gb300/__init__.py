@@ -92,6 +92,13 @@ def lib():
             "engram_gather_x": ([C, P, P, i64, i32, i64, P, P, P, P], ctypes.c_int),
             "engram_fuse_x": ([C, P, P, P, P, i64, P], ctypes.c_int),
             "engram_shard_rows": ([C, i32], i64),
+            "engram_host_cache_bytes": ([C, i64, i64], sz),
+            "engram_host_cache_reset": ([C, P, i64, i64, P], ctypes.c_int),
+            "engram_forward_host_cached_workspace_bytes": ([C, i64, i64], sz),
+            "engram_forward_host_cached": (
+                [C, P, P, i64, i32, i64, P, P, P, P, P, P, i64, i64, ctypes.c_uint32, P, sz, P, P, P, P, P],
+                ctypes.c_int,
+            ),
             "engram_gather_reduce_shard": ([C, i32, i32, P, P, i64, i32, i64, P, P, P, P], ctypes.c_int),
             "engram_forward_no_workspace": ([C, P, P, i64, i32, i64, P, P, P, P, P, P], ctypes.c_int),
             "engram_dedup_workspace_bytes": ([C], sz),
@@ -440,6 +447,65 @@ def engram_gather_reduce_shard(cfg, shard, n_shards, tokens, seq_offsets, tables
         "engram_gather_reduce_shard",
     )
     return mem
+
+
+def engram_host_cache_bytes(cfg, slots, capacity):
+    """Bytes of a row cache of `slots` rows (a power of two) plus `capacity` overflow rows."""
+    return int(lib().engram_host_cache_bytes(ctypes.byref(cfg), int(slots), int(capacity)))
+
+
+def engram_host_cache_new(cfg, slots, capacity, device=None, stream=None):
+    """A row cache on the device, reset (every slot empty)."""
+    n = engram_host_cache_bytes(cfg, slots, capacity)
+    if n == 0:
+        raise ValueError("slots must be a power of two and capacity >= 1")
+    cache = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    _check(lib().engram_host_cache_reset(ctypes.byref(cfg), _ptr(cache), int(slots), int(capacity), _stream(stream)),
+           "engram_host_cache_reset")
+    return cache
+
+
+def engram_forward_host_cached_workspace_bytes(cfg, n_query, capacity):
+    return int(lib().engram_forward_host_cached_workspace_bytes(ctypes.byref(cfg), n_query, capacity))
+
+
+def engram_forward_host_cached(cfg, tokens, seq_offsets, host_tables, host_scales, W_out, g, h, cache, slots,
+                               capacity, stamp, last_n=0, n_query=None, workspace=None, stats=None, stream=None,
+                               side_stream=None, ev_dedup=None, ev_staged=None):
+    """The host-table path with staged rows cached in HBM across calls.
+    `stamp` must be larger than every earlier call's on this cache since its
+    reset.  Returns stats int64 [4] on the device: distinct rows, cache hits,
+    rows staged over the host link, rows staged outside the cache."""
+    _need(tokens, torch.int32, "tokens")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(host_tables, torch.uint8, "host_tables", cuda=False)
+    _need(host_scales, torch.float32, "host_scales", cuda=False)
+    _need(h, torch.bfloat16, "h")
+    _need(cache, torch.uint8, "cache")
+    nq = _n_query(tokens, seq_offsets, last_n, n_query)
+    dev = h.device
+    if workspace is None:
+        workspace = torch.empty(engram_forward_host_cached_workspace_bytes(cfg, nq, capacity), dtype=torch.uint8,
+                                device=dev)
+    if stats is None:
+        stats = torch.zeros(4, dtype=torch.int64, device=dev)
+    if side_stream is None:
+        side_stream = torch.cuda.Stream(device=dev)
+    ev_dedup = ev_dedup or torch.cuda.Event()
+    ev_staged = ev_staged or torch.cuda.Event()
+    for ev in (ev_dedup, ev_staged):
+        if ev.cuda_event == 0:
+            ev.record(torch.cuda.current_stream() if stream is None else stream)
+    _check(
+        lib().engram_forward_host_cached(
+            ctypes.byref(cfg), _ptr(tokens), _ptr(seq_offsets), seq_offsets.numel() - 1, last_n, nq,
+            _ptr(host_tables), _ptr(host_scales), _ptr(W_out), _ptr(g), _ptr(h), _ptr(cache), int(slots),
+            int(capacity), int(stamp), _ptr(workspace), workspace.numel(), _ptr(stats), _stream(stream),
+            ctypes.c_void_p(side_stream.cuda_stream), ctypes.c_void_p(ev_dedup.cuda_event),
+            ctypes.c_void_p(ev_staged.cuda_event)),
+        "engram_forward_host_cached",
+    )
+    return stats
 
 
 def engram_dedup_workspace_bytes(cfg):

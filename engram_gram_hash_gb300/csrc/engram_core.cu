@@ -205,10 +205,11 @@ struct GatherParams {
 };
 
 // 4 blocks of 256 threads per SM (at most 64 registers a thread; 3 blocks and
-// 80 registers for kMx, which also holds twelve scale bytes a lane).  kMx: each row
+// 80 registers for kMx, which also holds twelve scale bytes a lane; 2 blocks
+// for the few-token form with gates, where occupancy does not matter).  kMx: each row
 // carries eight E8M0 block scales (one per 32 codes) instead of one fp32.
 template <int kMode, bool kBf16Out, bool kMx, bool kGate = false>
-__global__ void __launch_bounds__(256, kMx ? 3 : 4) gather_kernel(const __grid_constant__ GatherParams P) {
+__global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(const __grid_constant__ GatherParams P) {
     // The projection that consumes X may be launched as a programmatic
     // dependent: its CTAs take SMs as this grid's last blocks drain and start
     // on what does not depend on X.
@@ -594,14 +595,17 @@ __global__ void __launch_bounds__(256) dedup_remap_kernel(const int64_t *__restr
 // row pairs in flight, and the grid strides over the unique list.
 
 // kWhole: rows carrying block scales are staged whole (host_stride bytes).
+// dest: where list entry u goes in the staging buffers (nullptr: slot u).
 template <bool kWhole>
 __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ host_tables,
                                                     const float *__restrict__ host_scales, int64_t host_stride,
                                                     const int64_t *__restrict__ unique,
                                                     const int64_t *__restrict__ n_unique, int64_t capacity,
-                                                    uint8_t *__restrict__ staged, float *__restrict__ staged_scales) {
+                                                    uint8_t *__restrict__ staged, float *__restrict__ staged_scales,
+                                                    const int32_t *__restrict__ dest = nullptr) {
     const int64_t U = *n_unique;
     if (U > capacity) return;  // overflowed: the dedup flagged it and left no query pointing at a slot
+    auto D = [&](int64_t u) -> int64_t { return dest ? (int64_t)__ldg(dest + u) : u; };
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, c16 = lane & 15;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -626,9 +630,9 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
 #pragma unroll
             for (int k = 0; k < kPairs; ++k) {
                 const int64_t u = u0 + 2 * k + half;
-                if (flat[k] >= 0) *reinterpret_cast<uint4 *>(staged + u * host_stride + c16 * 16) = v[k];
+                if (flat[k] >= 0) *reinterpret_cast<uint4 *>(staged + D(u) * host_stride + c16 * 16) = v[k];
             }
-            if (has_tail) *reinterpret_cast<uint4 *>(staged + ut * host_stride + kRowBytes) = tail;
+            if (has_tail) *reinterpret_cast<uint4 *>(staged + D(ut) * host_stride + kRowBytes) = tail;
         } else {
             float sc[kPairs];
 #pragma unroll
@@ -642,11 +646,110 @@ __global__ void __launch_bounds__(256) stage_kernel(const uint8_t *__restrict__ 
             for (int k = 0; k < kPairs; ++k) {
                 const int64_t u = u0 + 2 * k + half;
                 if (flat[k] >= 0) {
-                    *reinterpret_cast<uint4 *>(staged + u * kRowBytes + c16 * 16) = v[k];
-                    if (c16 == 0) staged_scales[u] = sc[k];
+                    const int64_t du = D(u);
+                    *reinterpret_cast<uint4 *>(staged + du * kRowBytes + c16 * 16) = v[k];
+                    if (c16 == 0) staged_scales[du] = sc[k];
                 }
             }
         }
+    }
+}
+
+// =========================================================== row cache ==
+// Staged rows kept in HBM across calls (the hot rows of a Zipf token stream
+// are pulled over the host link once).  A direct-mapped cache of `slots`
+// rows (a power of two): row f lives in slot (f * 0x9E3779B97F4A7C15) >> (64 -
+// log2 slots), tagged with f.  Per call, each distinct row u of the batch
+// claims its slot with the call's stamp (atomicMax on the slot's claim word;
+// stamps increase from call to call): the first claimer of a slot this call
+// either finds its row there (a hit: nothing to stage) or takes the slot over
+// (a miss: staged into it, tag replaced); a row whose slot another row of the
+// same call already claimed is staged into the overflow rows after the
+// cache (slot `slots` + k).  where[u] is the row's slot for the gather.
+
+__device__ __forceinline__ int64_t cache_slot(int64_t flat, int log2_slots) {
+    return (int64_t)(((uint64_t)flat * kGolden) >> (64 - log2_slots));
+}
+
+__global__ void __launch_bounds__(256) cache_lookup_kernel(const int64_t *__restrict__ unique,
+                                                           const int64_t *__restrict__ n_unique, int64_t capacity,
+                                                           int64_t *__restrict__ tags, uint32_t *__restrict__ claims,
+                                                           int log2_slots, uint32_t stamp, int32_t *__restrict__ where,
+                                                           int64_t *__restrict__ stage_flat,
+                                                           int32_t *__restrict__ stage_dest,
+                                                           int64_t *__restrict__ stats) {
+    // stats: [0] distinct rows, [1] cache hits, [2] rows to stage, [3] overflow rows
+    const int64_t U = *n_unique;
+    if (blockIdx.x == 0 && threadIdx.x == 0) stats[0] = U;
+    if (U > capacity) return;  // the dedup overflowed and flagged it: nothing is staged or read
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    bool hit = false, stage = false, over = false;
+    int64_t flat = 0, dst = 0;
+    if (u < U) {
+        flat = __ldg(unique + u);
+        const int64_t s = cache_slot(flat, log2_slots);
+        const uint32_t old = atomicMax(claims + s, stamp);
+        if (old < stamp) {  // first this call: the slot is ours
+            dst = s;
+            if (tags[s] == flat) {
+                hit = true;
+            } else {
+                tags[s] = flat;
+                stage = true;
+            }
+        } else {
+            over = true;
+            stage = true;
+        }
+    }
+    // counters and stage-list positions: lanes within the warp (ballots),
+    // warps within the block (shared memory), one global atomic per block
+    __shared__ unsigned s_cnt[3];        // over, stage, hit: this block's totals
+    __shared__ unsigned long long s_base[2];
+    if (threadIdx.x < 3) s_cnt[threadIdx.x] = 0;
+    __syncthreads();
+    const unsigned m_over = __ballot_sync(0xffffffffu, over);
+    const unsigned m_stage = __ballot_sync(0xffffffffu, stage);
+    const unsigned m_hit = __ballot_sync(0xffffffffu, hit);
+    unsigned w_over = 0, w_stage = 0;
+    if (lane == 0) {
+        w_over = atomicAdd(&s_cnt[0], (unsigned)__popc(m_over));
+        w_stage = atomicAdd(&s_cnt[1], (unsigned)__popc(m_stage));
+        atomicAdd(&s_cnt[2], (unsigned)__popc(m_hit));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        s_base[0] = s_cnt[0] ? atomicAdd(reinterpret_cast<unsigned long long *>(stats + 3), (unsigned long long)s_cnt[0]) : 0;
+        s_base[1] = s_cnt[1] ? atomicAdd(reinterpret_cast<unsigned long long *>(stats + 2), (unsigned long long)s_cnt[1]) : 0;
+        if (s_cnt[2]) atomicAdd(reinterpret_cast<unsigned long long *>(stats + 1), (unsigned long long)s_cnt[2]);
+    }
+    __syncthreads();
+    w_over = __shfl_sync(0xffffffffu, w_over, 0);
+    w_stage = __shfl_sync(0xffffffffu, w_stage, 0);
+    const unsigned below = (1u << lane) - 1u;
+    if (over) dst = ((int64_t)1 << log2_slots) + (int64_t)(s_base[0] + w_over + __popc(m_over & below));
+    if (u < U) where[u] = (int32_t)dst;
+    if (stage) {
+        const int64_t k = (int64_t)(s_base[1] + w_stage + __popc(m_stage & below));
+        stage_flat[k] = flat;
+        stage_dest[k] = (int32_t)dst;
+    }
+}
+
+// idx_staged (dedup slots) -> cache slots
+__global__ void __launch_bounds__(256) cache_remap_kernel(int32_t *__restrict__ idx_staged, int64_t n,
+                                                          const int32_t *__restrict__ where) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n) return;
+    const int32_t u = idx_staged[g];
+    idx_staged[g] = u >= 0 ? __ldg(where + u) : kSlotNone;
+}
+
+__global__ void cache_reset_kernel(int64_t *__restrict__ tags, uint32_t *__restrict__ claims, int64_t slots) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < slots; i += (int64_t)gridDim.x * blockDim.x) {
+        tags[i] = -1;
+        claims[i] = 0;
     }
 }
 
@@ -817,14 +920,14 @@ engram_status dedup_launch(const engram_config *cfg, const int64_t *idx, int64_t
 // 256-byte rows plus fp32 scales.
 engram_status stage_launch(const uint8_t *host_tables, const float *host_scales, int64_t host_stride,
                            bool whole_rows, const int64_t *unique, const int64_t *n_unique, int64_t capacity,
-                           uint8_t *staged, float *staged_scales, cudaStream_t st) {
+                           uint8_t *staged, float *staged_scales, cudaStream_t st, const int32_t *dest = nullptr) {
     const int blocks = num_sms() * 8;
     if (whole_rows)
         stage_kernel<true><<<blocks, 256, 0, st>>>(host_tables, host_scales, host_stride, unique, n_unique, capacity,
-                                                   staged, staged_scales);
+                                                   staged, staged_scales, dest);
     else
         stage_kernel<false><<<blocks, 256, 0, st>>>(host_tables, host_scales, host_stride, unique, n_unique, capacity,
-                                                    staged, staged_scales);
+                                                    staged, staged_scales, dest);
     return launch_status();
 }
 
@@ -1458,6 +1561,150 @@ extern "C" engram_status engram_forward_host(const engram_config *cfg, const int
     if (cudaStreamWaitEvent(st, (cudaEvent_t)ev_staged, 0) != cudaSuccess) return ENGRAM_ECUDA;
     s = gather_launch(IDX_STAGED_I32, true, rows, mx(cfg) ? nullptr : sc, staged_stride(cfg), mx(cfg), idx_staged,
                       nullptr, n_query, capacity, X, st);
+    if (s != ENGRAM_OK) return s;
+    return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
+}
+
+// ============================================ host tables with a row cache ==
+
+struct CacheLayout {
+    size_t tags, claims, rows, scales, total;
+};
+
+static CacheLayout cache_layout(const engram_config *cfg, int64_t slots, int64_t capacity) {
+    CacheLayout L;
+    size_t o = 0;
+    L.tags = o;
+    o += round_up((size_t)slots * 8, 256);
+    L.claims = o;
+    o += round_up((size_t)slots * 4, 256);
+    L.rows = o;
+    o += round_up((size_t)(slots + capacity) * staged_stride(cfg), 256);
+    L.scales = o;
+    o += round_up((size_t)(slots + capacity) * 4, 256);
+    L.total = o;
+    return L;
+}
+
+static bool cache_args_ok(int64_t slots, int64_t capacity) {
+    return slots >= 1 && (slots & (slots - 1)) == 0 && capacity >= 1 && slots + capacity < (INT64_C(1) << 31);
+}
+
+extern "C" size_t engram_host_cache_bytes(const engram_config *cfg, int64_t slots, int64_t capacity) {
+    if (check_config(cfg) != ENGRAM_OK || !cache_args_ok(slots, capacity)) return 0;
+    return cache_layout(cfg, slots, capacity).total;
+}
+
+extern "C" engram_status engram_host_cache_reset(const engram_config *cfg, void *cache, int64_t slots,
+                                                 int64_t capacity, void *stream) {
+    if (check_config(cfg) != ENGRAM_OK || !cache_args_ok(slots, capacity) || !cache || !aligned(cache, 256))
+        return ENGRAM_EINVAL;
+    const CacheLayout L = cache_layout(cfg, slots, capacity);
+    uint8_t *c = static_cast<uint8_t *>(cache);
+    const unsigned blocks = (unsigned)std::min<int64_t>((slots + 255) / 256, (int64_t)num_sms() * 8);
+    cache_reset_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(reinterpret_cast<int64_t *>(c + L.tags),
+                                                                 reinterpret_cast<uint32_t *>(c + L.claims), slots);
+    return launch_status();
+}
+
+// workspace: idx [n][48] i64 | idx_staged [n][48] i32 | X [n][512] bf16 |
+// unique [cap] i64 | where [cap] i32 | stage_flat [cap] i64 | stage_dest [cap]
+// i32 | n_unique i64 | dedup workspace
+struct CachedLayout {
+    size_t idx, idx_staged, x, unique, where, stage_flat, stage_dest, n_unique, dedup, total;
+};
+
+static CachedLayout cached_layout(const engram_config *cfg, int64_t n, int64_t cap) {
+    CachedLayout L;
+    size_t o = 0;
+    L.idx = o;
+    o += round_up((size_t)n * kTables * 8, 256);
+    L.idx_staged = o;
+    o += round_up((size_t)n * kTables * 4, 256);
+    L.x = o;
+    o += round_up((size_t)n * kMem * 2, 256);
+    L.unique = o;
+    o += round_up((size_t)cap * 8, 256);
+    L.where = o;
+    o += round_up((size_t)cap * 4, 256);
+    L.stage_flat = o;
+    o += round_up((size_t)cap * 8, 256);
+    L.stage_dest = o;
+    o += round_up((size_t)cap * 4, 256);
+    L.n_unique = o;
+    o += 256;
+    L.dedup = o;
+    o += dedup_bytes(cfg);
+    L.total = o;
+    return L;
+}
+
+extern "C" size_t engram_forward_host_cached_workspace_bytes(const engram_config *cfg, int64_t n_query,
+                                                             int64_t capacity) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || capacity < 1) return 0;
+    return cached_layout(cfg, n_query, capacity).total;
+}
+
+extern "C" engram_status engram_forward_host_cached(const engram_config *cfg, const int32_t *tokens,
+                                                    const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                                    int64_t n_query, const uint8_t *host_tables,
+                                                    const float *host_scales, const uint16_t *W_out, const uint16_t *g,
+                                                    uint16_t *h, void *cache, int64_t slots, int64_t capacity,
+                                                    uint32_t stamp, void *workspace, size_t workspace_bytes,
+                                                    int64_t *stats, void *stream, void *side_stream, void *ev_dedup,
+                                                    void *ev_staged) {
+    if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;
+    if (!cache_args_ok(slots, capacity) || stamp == 0) return ENGRAM_EINVAL;
+    if (n_query == 0) return ENGRAM_OK;
+    if (!tokens || !seq_offsets || n_seqs < 1 || !host_tables || !scales_ok(cfg, host_scales) || !workspace ||
+        !cache || !stats || !ev_dedup || !ev_staged)
+        return ENGRAM_EINVAL;
+    if (last_n > 0 && n_query != n_seqs * (int64_t)last_n) return ENGRAM_EINVAL;
+    if (check_fuse_args(cfg, W_out, g, h) != ENGRAM_OK) return ENGRAM_EINVAL;
+    if (!aligned(host_tables, 16) || !aligned(workspace, 256) || !aligned(cache, 256) || !aligned(stats, 8))
+        return ENGRAM_EINVAL;
+    if (n_query * kTables >= (INT64_C(1) << 31)) return ENGRAM_EINVAL;
+    const CachedLayout L = cached_layout(cfg, n_query, capacity);
+    if (workspace_bytes < L.total) return ENGRAM_ENOMEM;
+    cudaStream_t st = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int64_t *idx = reinterpret_cast<int64_t *>(ws + L.idx);
+    int32_t *idx_staged = reinterpret_cast<int32_t *>(ws + L.idx_staged);
+    uint16_t *X = reinterpret_cast<uint16_t *>(ws + L.x);
+    int64_t *unique = reinterpret_cast<int64_t *>(ws + L.unique);
+    int32_t *where = reinterpret_cast<int32_t *>(ws + L.where);
+    int64_t *stage_flat = reinterpret_cast<int64_t *>(ws + L.stage_flat);
+    int32_t *stage_dest = reinterpret_cast<int32_t *>(ws + L.stage_dest);
+    int64_t *n_unique = reinterpret_cast<int64_t *>(ws + L.n_unique);
+    const CacheLayout C = cache_layout(cfg, slots, capacity);
+    uint8_t *cb = static_cast<uint8_t *>(cache);
+    int log2_slots = 0;
+    while ((INT64_C(1) << log2_slots) < slots) ++log2_slots;
+
+    engram_status s = hash_launch(cfg, tokens, seq_offsets, n_seqs, last_n, n_query, idx, st);
+    if (s != ENGRAM_OK) return s;
+    s = dedup_launch(cfg, idx, n_query, ws + L.dedup, unique, capacity, idx_staged, n_unique, st);
+    if (s != ENGRAM_OK) return s;
+    if (cudaMemsetAsync(stats, 0, 4 * sizeof(int64_t), st) != cudaSuccess) return ENGRAM_ECUDA;
+    cache_lookup_kernel<<<(unsigned)((capacity + 255) / 256), 256, 0, st>>>(
+        unique, n_unique, capacity, reinterpret_cast<int64_t *>(cb + C.tags), reinterpret_cast<uint32_t *>(cb + C.claims),
+        log2_slots, stamp, where, stage_flat, stage_dest, stats);
+    s = launch_status();
+    if (s != ENGRAM_OK) return s;
+    if (cudaEventRecord((cudaEvent_t)ev_dedup, st) != cudaSuccess) return ENGRAM_ECUDA;
+    if (cudaStreamWaitEvent(side, (cudaEvent_t)ev_dedup, 0) != cudaSuccess) return ENGRAM_ECUDA;
+    // the misses and overflow rows, from pinned host memory into their slots
+    s = stage_launch(host_tables, scales_arg(cfg, host_scales), row_stride(cfg), mx(cfg), stage_flat, stats + 2,
+                     capacity, cb + C.rows, reinterpret_cast<float *>(cb + C.scales), side, stage_dest);
+    if (s != ENGRAM_OK) return s;
+    if (cudaEventRecord((cudaEvent_t)ev_staged, side) != cudaSuccess) return ENGRAM_ECUDA;
+    const int64_t n = n_query * kTables;
+    cache_remap_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx_staged, n, where);
+    s = launch_status();
+    if (s != ENGRAM_OK) return s;
+    if (cudaStreamWaitEvent(st, (cudaEvent_t)ev_staged, 0) != cudaSuccess) return ENGRAM_ECUDA;
+    s = gather_launch(IDX_STAGED_I32, true, cb + C.rows, mx(cfg) ? nullptr : reinterpret_cast<float *>(cb + C.scales),
+                      staged_stride(cfg), mx(cfg), idx_staged, nullptr, n_query, slots + capacity, X, st);
     if (s != ENGRAM_OK) return s;
     return fuse_launch(cfg, nullptr, X, W_out, g, h, n_query, st);
 }

@@ -341,6 +341,46 @@ engram_status engram_host_alloc(size_t bytes, void **ptr);
 engram_status engram_host_free(void *ptr);
 
 /*
+ * The host-table path with a cache of staged rows kept in HBM across calls
+ * (the pages' staging of hot rows for a Zipf token stream, "Engram: the table
+ * that is never multiplied" and "What makes up the 511 GB of weights?": rows
+ * pulled over the host link once are read from device memory afterwards).
+ * The cache is a caller-owned device buffer of
+ * engram_host_cache_bytes(cfg, slots, capacity) bytes (256-byte aligned):
+ * `slots` cached rows (a power of two, direct-mapped by the row's flat index
+ * j*R + row) plus `capacity` overflow rows, with their tags.
+ * engram_host_cache_reset empties it (enqueued on `stream`).
+ * engram_forward_host_cached: hash and dedup as engram_forward_host; then
+ * every distinct row of the batch claims its cache slot for this call (the
+ * first claimant owns it: a row already there is a hit and is not staged, any
+ * other row replaces it); a row whose slot another row of the same call owns
+ * goes to an overflow row.  Only misses cross the host link (on
+ * `side_stream`, after `ev_dedup`); the staged gather reads cache and
+ * overflow rows and the projection follows on `stream` (after `ev_staged`).
+ * h equals engram_forward's on the same tables bit for bit.
+ *   stamp    >= 1, larger than every earlier call's on this cache since its
+ *            reset (a call counter); a cache serves one stream of calls:
+ *            calls that overlap on the GPU race on it
+ *   capacity distinct rows per call at most (n_query * 48 always suffices);
+ *            more set ENGRAM_ECAPACITY, stage nothing and leave h unchanged
+ *   stats    int64 [4] (device): distinct rows, cache hits, rows staged over
+ *            the host link, of which outside the cache (overflow)
+ * workspace >= engram_forward_host_cached_workspace_bytes(cfg, n_query,
+ * capacity); host tables and scales as in engram_forward_host.
+ */
+size_t engram_host_cache_bytes(const engram_config *cfg, int64_t slots, int64_t capacity);
+engram_status engram_host_cache_reset(const engram_config *cfg, void *cache, int64_t slots, int64_t capacity,
+                                      void *stream);
+size_t engram_forward_host_cached_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t capacity);
+engram_status engram_forward_host_cached(const engram_config *cfg, const int32_t *tokens,
+                                         const int64_t *seq_offsets, int64_t n_seqs, int32_t last_n,
+                                         int64_t n_query, const uint8_t *host_tables, const float *host_scales,
+                                         const uint16_t *W_out, const uint16_t *g, uint16_t *h, void *cache,
+                                         int64_t slots, int64_t capacity, uint32_t stamp, void *workspace,
+                                         size_t workspace_bytes, int64_t *stats, void *stream, void *side_stream,
+                                         void *ev_dedup, void *ev_staged);
+
+/*
  * The host-table path pipelined over chunks of `chunk` query tokens (the
  * pages' background prefetch of host rows on a side stream, "Engram: the table
  * that is never multiplied", applied chunk by chunk).  All queries are hashed

@@ -74,3 +74,50 @@ def check_all_tokens(cfg, seeds, tok, offs, qpos, gpu_mem, gpu_h, chunk=512, pro
         "seconds": secs,
         "procs": procs,
     }
+
+
+# ------------------------------------------------- the per-layer form -------
+
+def _init_layer(seed, d, eps, V, R, seeds, tok, offs, qpos, module):
+    wq, wk, wm = host.layer_weights(seed, d, module)
+    lut = np.array([abs(oracle.e4m3_value(c)) if c not in (0x7F, 0xFF) else 0.0 for c in range(256)])
+    _W.update(seed=seed, d=d, eps=eps, V=V, R=R, seeds=seeds, tok=tok, offs=offs, qpos=qpos, module=module,
+              wq=wq, wk=wk, wm=wm, abs_lut=lut)
+
+
+def _check_layer_chunk(job):
+    q, h_in, h_gpu, x_gpu = job
+    w = _W
+    m = w["module"]
+    q = np.asarray(q, np.int64)
+    idx = oracle.hash_positions(w["tok"], w["offs"], w["V"], w["R"], w["seeds"], w["qpos"][q])
+    jj = np.tile(np.arange(24 * m, 24 * m + 24), len(q))
+    r = idx[:, 24 * m:24 * m + 24].reshape(-1)
+    codes = host.table_rows(w["seed"], jj, r).reshape(len(q), 24, 256)
+    sc = host.scales(w["seed"], jj, r).reshape(len(q), 24)
+    hn, _, e = oracle.layer_gated(codes, sc, w["wq"], w["wk"], w["wm"], h_in, w["eps"])
+    bound = (w["abs_lut"][codes] * sc[:, :, None].astype(np.float64)).sum(axis=1)  # sum_j |r_j|
+    g, ref = _bf16_f64(h_gpu), _bf16_f64(hn)
+    h_rel = np.abs(g - ref) / np.maximum(1.0, np.abs(ref))
+    x_err = np.abs(_bf16_f64(x_gpu) - e)
+    x_bad = x_err > 1e-3 * bound + 2.0**-8 * np.abs(e) + 1e-30
+    return len(q), float(h_rel.max()), int((h_rel > H_TOL).sum()), int(x_bad.sum())
+
+
+def check_layer_all_tokens(cfg, seeds, tok, offs, qpos, module, h_in, h_gpu, x_gpu, chunk=256, procs=None):
+    """One Engram layer on every query token: h_gpu (bf16 bits [Tq,d]) against
+    the oracle applied to h_in (the GPU's h before the layer), and the
+    layer's X (bf16 bits [Tq,256]) against the oracle's gated sum.  Returns a
+    summary dict; the caller asserts."""
+    tq = h_gpu.shape[0]
+    procs = procs or os.cpu_count() or 1
+    oracle.build()
+    jobs = ((np.arange(a, min(a + chunk, tq)), h_in[a:a + chunk], h_gpu[a:a + chunk], x_gpu[a:a + chunk])
+            for a in range(0, tq, chunk))
+    t0 = time.time()
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(procs, initializer=_init_layer,
+                  initargs=(cfg.seed, cfg.d, cfg.rms_eps, cfg.V, cfg.R, seeds, tok, offs, qpos, module)) as pool:
+        res = list(pool.imap_unordered(_check_layer_chunk, jobs))
+    return {"tokens": sum(r[0] for r in res), "h_worst": max(r[1] for r in res), "h_bad": sum(r[2] for r in res),
+            "x_bad": sum(r[3] for r in res), "seconds": time.time() - t0, "procs": procs}

@@ -114,6 +114,13 @@ def test_invalid_arguments_rejected_before_any_device_work(eg):
     # workspace too small
     assert lib.engram_dedup(ctypes.byref(c), ctypes.c_void_p(256), 4, ctypes.c_void_p(256), 16,
                             ctypes.c_void_p(256), 100, ctypes.c_void_p(256), ctypes.c_void_p(256), null) == 6
+    # row cache: slots must be a power of two; a call needs a stamp >= 1
+    assert lib.engram_host_cache_bytes(ctypes.byref(c), 1000, 10) == 0
+    assert lib.engram_host_cache_bytes(ctypes.byref(c), 1024, 10) >= 1034 * 260
+    assert lib.engram_host_cache_reset(ctypes.byref(c), ctypes.c_void_p(256), 1000, 10, null) == 1
+    p256 = ctypes.c_void_p(256)
+    assert lib.engram_forward_host_cached(ctypes.byref(c), p256, p256, 1, 0, 4, p256, p256, p256, p256, p256, p256,
+                                          1024, 10, 0, p256, 1 << 30, p256, null, null, p256, p256) == 1
     # no-workspace entry: a malformed call is EINVAL even when it is also too large;
     # a well-formed call past the scratch limit is ENOMEM (both before any device work)
     big = 16384 + 1

@@ -199,6 +199,32 @@ def test_layers_many_tiles_persistent_loop(eg):
         assert np.all(err <= 1e-3 * bounds[0] + 2.0**-8 * np.abs(es[0]) + 1e-30), (m, float(err.max()))
 
 
+def test_layers_every_token_large(eg):
+    """The per-layer form on the full large workload (131,072 tokens, 103 GB
+    of tables, the benchmark's --variant layers call): each layer on EVERY
+    query token against the oracle applied to the GPU's h before that layer
+    (every host core, spawned processes)."""
+    from oracle_pool import check_layer_all_tokens
+
+    cfg = CONFIGS["large"]
+    w = Workload(cfg)
+    nq = cfg.tq
+    h = w.fresh_h()
+    ws = torch.empty(eg.engram_layer_workspace_bytes(w.c, nq), dtype=torch.uint8, device="cuda")
+    for m in (0, 1):
+        h_in = _bits(h)
+        wq, wk, wm = _weights(eg, cfg, m)
+        wkk = eg.engram_layer_keys(w.c, wk)
+        eg.engram_layer_forward(w.c, m, w.tokens, w.seq_offsets, w.tables, w.scales, wq, wkk, wm, h, n_query=nq,
+                                workspace=ws)
+        torch.cuda.synchronize()
+        assert eg.engram_last_error() == 0
+        X = _bits(eg.layer_workspace_views(ws, nq)[2])
+        r = check_layer_all_tokens(cfg, w.seeds, w.tok, w.offs, w.qpos, m, h_in, _bits(h), X)
+        print(f"layer {m}: {r}")
+        assert r["tokens"] == nq and r["h_bad"] == 0 and r["x_bad"] == 0, r
+
+
 def test_layer_record_layout_same_bits(eg):
     """Rows that carry their scale give the same h bits."""
     cfg = CASES["prefill_small"]
