@@ -800,6 +800,18 @@ static engram_status cuda_fail(cudaError_t e, const char *what) {
     return ENGRAM_ECUDA;
 }
 
+// Opt a kernel in to `bytes` of dynamic shared memory once per device.
+static engram_status ensure_smem(const void *kern, int bytes, std::atomic<bool> *attr_done) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(smem)");
+        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
+    }
+    return ENGRAM_OK;
+}
+
 engram_status launch_status() {
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ENGRAM_OK : cuda_fail(e, "kernel launch");
@@ -1157,11 +1169,17 @@ engram_status fuse_launch(const engram_config *cfg, const float *mem, const uint
     return fuse_dispatch<FUSE_F32_MEM>(wmap, xmap, xmap, p, st);
 }
 
+static engram_status narrow_layer_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W, uint16_t *h,
+                                         int64_t n_query, cudaStream_t st);
+static bool narrow_fits(int64_t m_tiles, int d);
+
 // One Engram layer's projection: h = bf16(h + X W_m), X [n][256] bf16,
-// W_m [256][d] (fuse2 with 4 K-blocks and no token gate).
+// W_m [256][d] (fuse2 with 4 K-blocks and no token gate; the d-split kernel
+// when the batch fits one wave of 64-column CTAs).
 static engram_status layer_projection_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W,
                                              uint16_t *h, int64_t n_query, cudaStream_t st) {
     const int d = cfg->d_model;
+    if (narrow_fits((n_query + fuse::BM - 1) / fuse::BM, d)) return narrow_layer_launch(cfg, X, W, h, n_query, st);
     const int n_chunks = d / fuse::BN;
     fuse::Params p;
     memset(&p, 0, sizeof(p));
@@ -1186,10 +1204,28 @@ static engram_status layer_projection_launch(const engram_config *cfg, const uin
 // out = s * (A @ B) on tcgen05 (layer::query_kernel): A bf16 [n][K], B bf16
 // [K][256]; with RMS s = rinv(A row), with SPLIT out is bf16 [n][512] (hi | lo)
 // instead of fp32 [n][256].
+// K split for the per-layer query products of few tiles: the largest of
+// 16, 8, 4, 2 that divides the K-blocks into runs of at least 2 with every
+// (tile, run) on its own SM; 1 (no split) for batches of more than a quarter
+// of the SM count in tiles.
+static int query_splits(int64_t m_tiles, int k) {
+    const int kb = k / layer::BK;
+    if (m_tiles * 4 > num_sms()) return 1;
+    for (int s = 16; s >= 2; s /= 2)
+        if (kb % s == 0 && kb / s >= 2 && m_tiles * s <= num_sms()) return s;
+    return 1;
+}
+
+// out = s * (A @ B) on tcgen05 (layer::query_kernel): A bf16 [n][K], B bf16
+// [K][256]; with RMS s = rinv(A row), with SPLIT out is bf16 [n][512] (hi | lo)
+// instead of fp32 [n][256].  splits > 1: K split over that many CTAs per tile
+// into `part` (fp32 [splits][n][256] + [splits][n]), then added up by
+// query_reduce_kernel.
 template <bool RMS, bool SPLIT>
 static engram_status query_launch(const engram_config *cfg, const uint16_t *A, int K, const uint16_t *B, void *out,
-                                  int64_t n_query, cudaStream_t st) {
+                                  int64_t n_query, cudaStream_t st, int splits = 1, float *part = nullptr) {
     layer::QParams p;
+    memset(&p, 0, sizeof(p));
     p.out = out;
     p.n_query = n_query;
     p.m_tiles = (n_query + layer::BM - 1) / layer::BM;
@@ -1200,15 +1236,27 @@ static engram_status query_launch(const engram_config *cfg, const uint16_t *A, i
         return cuda_fail(cudaErrorInvalidValue, "query A map");
     if (!bf16_map_2d(&bmap, B, kLayerWidth, (uint64_t)K, 64, layer::BK))
         return cuda_fail(cudaErrorInvalidValue, "query B map");
-    auto kern = layer::query_kernel<RMS, SPLIT>;
-    static std::atomic<bool> attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, layer::SMEM_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(query smem)");
-        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
+    if (splits > 1) {
+        static std::atomic<bool> attr_split[64] = {};
+        auto kern = layer::query_kernel<RMS, false, true>;
+        engram_status s = ensure_smem((const void *)kern, layer::SMEM_BYTES, attr_split);
+        if (s != ENGRAM_OK) return s;
+        p.out = part;
+        p.ss_out = part + (size_t)splits * n_query * kLayerWidth;
+        p.kb_per_split = K / layer::BK / splits;
+        const dim3 grid((unsigned)p.m_tiles, (unsigned)splits);
+        kern<<<grid, layer::NUM_THREADS, layer::SMEM_BYTES, st>>>(amap, bmap, p);
+        s = launch_status();
+        if (s != ENGRAM_OK) return s;
+        const int64_t threads = n_query * (kLayerWidth / 4);
+        layer::query_reduce_kernel<RMS, SPLIT><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+            part, p.ss_out, splits, n_query, K, cfg->rms_eps, out);
+        return launch_status();
     }
+    static std::atomic<bool> attr_done[64] = {};
+    auto kern = layer::query_kernel<RMS, SPLIT>;
+    engram_status s = ensure_smem((const void *)kern, layer::SMEM_BYTES, attr_done);
+    if (s != ENGRAM_OK) return s;
     const unsigned grid = (unsigned)std::min<int64_t>(p.m_tiles, num_sms());
     kern<<<grid, layer::NUM_THREADS, layer::SMEM_BYTES, st>>>(amap, bmap, p);
     return launch_status();
@@ -1277,26 +1325,26 @@ static engram_status gather_gate_launch(const engram_config *cfg, const uint8_t 
     return launch_status();
 }
 
-// h = bf16(h + gate * X W_out) by the d-split kernel, launched as a
-// programmatic dependent of the gather_gate_launch just enqueued on `st`.
-static engram_status narrow_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W, const float *gate,
-                                   uint16_t *h, int64_t n_query, cudaStream_t st) {
+// h = bf16(h + gate * X W) (gate != nullptr, X [n][512]) or h = bf16(h + X W)
+// (gate == nullptr: one Engram layer, X [n][256]) by the d-split kernel,
+// launched as a programmatic dependent of the kernel just enqueued on `st`
+// (which writes X and the gates but not h or W).
+template <int KBLK, bool GATED>
+static engram_status narrow_launch_t(const engram_config *cfg, const uint16_t *X, const uint16_t *W, const float *gate,
+                                     uint16_t *h, int64_t n_query, cudaStream_t st) {
     const int d = cfg->d_model;
+    const int k = KBLK * narrow::BK;
     CUtensorMap wmap, xmap, hl, hs;
-    if (!bf16_map_2d(&wmap, W, (uint64_t)d, kMem, narrow::BN, narrow::BK) ||
-        !bf16_map_2d(&xmap, X, kMem, (uint64_t)n_query, narrow::BK, narrow::BM) ||
+    if (!bf16_map_2d(&wmap, W, (uint64_t)d, (uint64_t)k, narrow::BN, narrow::BK) ||
+        !bf16_map_2d(&xmap, X, (uint64_t)k, (uint64_t)n_query, narrow::BK, narrow::BM) ||
         !bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, narrow::BM) ||
         !bf16_map_2d(&hs, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, 32))
         return cuda_fail(cudaErrorInvalidValue, "narrow projection tensor maps");
     static std::atomic<bool> attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(narrow::narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, narrow::SMEM_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(narrow smem)");
-        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
-    }
+    auto kern = narrow::narrow_kernel<KBLK, GATED>;
+    constexpr int smem = narrow::smem_bytes<KBLK>();
+    engram_status s = ensure_smem((const void *)kern, smem, attr_done);
+    if (s != ENGRAM_OK) return s;
     narrow::Params p;
     p.gate = gate;
     p.n_query = n_query;
@@ -1306,13 +1354,23 @@ static engram_status narrow_launch(const engram_config *cfg, const uint16_t *X, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.gridDim = dim3((unsigned)(d / narrow::BN), (unsigned)((n_query + narrow::BM - 1) / narrow::BM));
     lc.blockDim = dim3(narrow::NUM_THREADS);
-    lc.dynamicSmemBytes = narrow::SMEM_BYTES;
+    lc.dynamicSmemBytes = smem;
     lc.stream = st;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&lc, narrow::narrow_kernel, wmap, xmap, hl, hs, p);
+    const cudaError_t le = cudaLaunchKernelEx(&lc, kern, wmap, xmap, hl, hs, p);
     if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(narrow)");
     return launch_status();
+}
+
+static engram_status narrow_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W, const float *gate,
+                                   uint16_t *h, int64_t n_query, cudaStream_t st) {
+    return narrow_launch_t<kMem / narrow::BK, true>(cfg, X, W, gate, h, n_query, st);
+}
+
+static engram_status narrow_layer_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W, uint16_t *h,
+                                         int64_t n_query, cudaStream_t st) {
+    return narrow_launch_t<kLayerWidth / narrow::BK, false>(cfg, X, W, nullptr, h, n_query, st);
 }
 
 }  // namespace engram
@@ -1778,10 +1836,20 @@ extern "C" engram_status engram_layer_keys(const engram_config *cfg, const uint1
 // workspace: q pair bf16 [n][512] | u fp32 [n][256] | X bf16 [n][256]
 static size_t layer_off_u(int64_t n) { return round_up((size_t)n * 2 * kLayerWidth * 2, 256); }
 static size_t layer_off_x(int64_t n) { return layer_off_u(n) + round_up((size_t)n * kLayerWidth * 4, 256); }
+static size_t layer_off_part(int64_t n) { return layer_off_x(n) + round_up((size_t)n * kLayerWidth * 2, 256); }
+// the split-K partial products of the two query products (few tiles only)
+static int layer_max_splits(const engram_config *cfg, int64_t n) {
+    const int64_t m_tiles = (n + layer::BM - 1) / layer::BM;
+    return std::max(query_splits(m_tiles, cfg->d_model), query_splits(m_tiles, 2 * kLayerWidth));
+}
+static size_t layer_part_bytes(const engram_config *cfg, int64_t n) {
+    const int s = layer_max_splits(cfg, n);
+    return s > 1 ? round_up((size_t)s * n * (kLayerWidth + 1) * 4, 256) : 0;
+}
 
 extern "C" size_t engram_layer_workspace_bytes(const engram_config *cfg, int64_t n_query) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0) return 0;
-    return layer_off_x(n_query) + round_up((size_t)n_query * kLayerWidth * 2, 256);
+    return layer_off_part(n_query) + layer_part_bytes(cfg, n_query);
 }
 
 extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t module, const int32_t *tokens,
@@ -1810,9 +1878,13 @@ extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t 
     float *u = reinterpret_cast<float *>(ws + layer_off_u(n_query));
     uint16_t *X = reinterpret_cast<uint16_t *>(ws + layer_off_x(n_query));
     // q = rinv(h) h W_q as a bf16 pair, then u = [q_hi | q_lo] [W_k^T ; W_k^T]
-    engram_status s = query_launch<true, true>(cfg, h, d, W_q, qpair, n_query, st);
+    // (few tiles: K split over several CTAs per tile, partial products added up)
+    const int64_t m_tiles = (n_query + layer::BM - 1) / layer::BM;
+    float *part = reinterpret_cast<float *>(ws + layer_off_part(n_query));
+    engram_status s = query_launch<true, true>(cfg, h, d, W_q, qpair, n_query, st, query_splits(m_tiles, d), part);
     if (s != ENGRAM_OK) return s;
-    s = query_launch<false, false>(cfg, qpair, 2 * kLayerWidth, W_kk, u, n_query, st);
+    s = query_launch<false, false>(cfg, qpair, 2 * kLayerWidth, W_kk, u, n_query, st,
+                                   query_splits(m_tiles, 2 * kLayerWidth), part);
     if (s != ENGRAM_OK) return s;
     GatedParams P;
     memset(&P, 0, sizeof(P));

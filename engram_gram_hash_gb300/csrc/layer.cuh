@@ -44,10 +44,13 @@ constexpr int NUM_THREADS = 32 * 12;
 constexpr uint32_t IDESC = idesc_bf16(BM, BN, /*b_mn_major=*/true);
 
 struct QParams {
-    void *out;  // fp32 [n_query][256], or bf16 [n_query][512] (hi | lo) with SPLIT
+    void *out;  // fp32 [n_query][256], or bf16 [n_query][512] (hi | lo) with SPLIT;
+                // with SPLITK fp32 partial products [splits][n_query][256]
+    float *ss_out;  // SPLITK with RMS: partial sum(A^2) [splits][n_query]
     int64_t n_query;
     int64_t m_tiles;
     int32_t d;
+    int32_t kb_per_split;  // SPLITK: K-blocks per CTA (gridDim.y = splits)
     float eps;
 };
 
@@ -67,7 +70,10 @@ struct QShared {
 constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + (int)sizeof(QShared);
 static_assert(SMEM_BYTES <= 232448, "query kernel shared memory over the per-CTA limit");
 
-template <bool RMS, bool SPLIT>
+// SPLITK (few tiles): CTA (x, y) takes tile x and the y-th run of
+// kb_per_split K-blocks, and writes its raw fp32 partial product (and, with
+// RMS, its partial sum(A^2)) for query_reduce_kernel to add up in split order.
+template <bool RMS, bool SPLIT, bool SPLITK = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     query_kernel(const __grid_constant__ CUtensorMap h_map, const __grid_constant__ CUtensorMap w_map,
                  const __grid_constant__ QParams p) {
@@ -81,7 +87,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int *abort = &sh->abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int KB = p.d / BK;
+    const int kb0 = SPLITK ? (int)blockIdx.y * p.kb_per_split : 0;
+    const int kb1 = SPLITK ? kb0 + p.kb_per_split : p.d / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool issued[NSTAGE] = {};
             uint32_t issued_parity[NSTAGE] = {};
             for (int64_t mt = blockIdx.x; mt < p.m_tiles && !*abort; mt += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort)) break;
                     mbar_arrive_expect_tx(&sh->full[stage], STAGE_BYTES);
                     uint8_t *dst = ring + stage * STAGE_BYTES;
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(&sh->acc_empty[buf], ((it >> 1) & 1u) ^ 1u, abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&sh->full[stage], phase, abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st_addr = ring_addr + stage * STAGE_BYTES;
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t adesc = smem_desc(st_addr + s * 32, 16, 1024, kSwizzle128B);
                         const uint64_t bdesc =
                             smem_desc(st_addr + H_KBLOCK_BYTES + s * 2048, W_BOX_BYTES, 1024, kSwizzle128B);
-                        mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | s) != 0);
+                        mma_bf16(d_tmem, adesc, bdesc, IDESC, ((kb - kb0) | s) != 0);
                     }
                     mma_commit(&sh->empty[stage]);
                     if (++stage == NSTAGE) {
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (it >= 2 && !mbar_wait(&sh->rs_free[b], ((it >> 1) - 1u) & 1u, abort)) break;
             float ss = 0.f;
             bool ok = true;
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(&sh->full[stage], phase, abort)) { ok = false; break; }
                 const uint32_t rbase = ring_addr + stage * STAGE_BYTES + row * 128;
 #pragma unroll
@@ -210,7 +217,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            sh->rinv[b][row] = RMS ? rsqrtf(ss / (float)p.d + p.eps) : 1.f;
+            if (SPLITK) {  // the partial sum goes out; the products stay unscaled
+                const int64_t t = mt * BM + row;
+                if (RMS && t < p.n_query) p.ss_out[(int64_t)blockIdx.y * p.n_query + t] = ss;
+                sh->rinv[b][row] = 1.f;
+            } else {
+                sh->rinv[b][row] = RMS ? rsqrtf(ss / (float)p.d + p.eps) : 1.f;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->rs_full[b]);
         }
@@ -232,7 +245,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + c32 * 32, y);
                 tmem_ld_wait();
                 if (t < p.n_query) {
-                    if constexpr (SPLIT) {  // bf16 hi at column c, lo at column 256 + c
+                    if constexpr (SPLITK) {  // this split's raw partial product
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) +
+                                                                 ((int64_t)blockIdx.y * p.n_query + t) * BN + c32 * 32);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = make_float4(__uint_as_float(y[4 * k]), __uint_as_float(y[4 * k + 1]),
+                                                 __uint_as_float(y[4 * k + 2]), __uint_as_float(y[4 * k + 3]));
+                    } else if constexpr (SPLIT) {  // bf16 hi at column c, lo at column 256 + c
                         uint4 *hi = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + t * 2 * BN + c32 * 32);
                         uint4 *lo = hi + BN / 8;
 #pragma unroll
@@ -271,6 +291,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// The split-K products added up in split order: out = s * sum_y part[y], s =
+// rinv(sum_y ss[y]) with RMS; written as fp32 [n][256] or, with SPLIT, as the
+// bf16 pair [n][512] = [hi | lo].  A thread per (token, 4 columns).
+template <bool RMS, bool SPLIT>
+__global__ void __launch_bounds__(256) query_reduce_kernel(const float *__restrict__ part,
+                                                           const float *__restrict__ ss, int splits, int64_t n,
+                                                           int32_t d, float eps, void *out) {
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n * (BN / 4)) return;
+    const int64_t t = g / (BN / 4);
+    const int c = (int)(g - t * (BN / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float s2 = 0.f;
+    for (int y = 0; y < splits; ++y) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(part + ((int64_t)y * n + t) * BN + c));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+        if (RMS) s2 += __ldg(ss + (int64_t)y * n + t);
+    }
+    const float rinv = RMS ? rsqrtf(s2 / (float)d + eps) : 1.f;
+    const float v[4] = {acc.x * rinv, acc.y * rinv, acc.z * rinv, acc.w * rinv};
+    if constexpr (SPLIT) {
+        uint16_t *hi = static_cast<uint16_t *>(out) + t * 2 * BN + c;
+        const uint32_t h01 = pack_bf16x2(v[0], v[1]), h23 = pack_bf16x2(v[2], v[3]);
+        const uint32_t l01 = pack_bf16x2(v[0] - bf16_lo(h01), v[1] - bf16_hi(h01));
+        const uint32_t l23 = pack_bf16x2(v[2] - bf16_lo(h23), v[3] - bf16_hi(h23));
+        *reinterpret_cast<uint2 *>(hi) = make_uint2(h01, h23);
+        *reinterpret_cast<uint2 *>(hi + BN) = make_uint2(l01, l23);
+    } else {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + t * BN + c) = make_float4(v[0], v[1], v[2], v[3]);
     }
 }
 

@@ -1,4 +1,4 @@
-// The gated projection for few tokens (decode): d split over many CTAs.
+// The projection for few tokens (decode): d split over many CTAs.
 //
 // With one or two tiles of 128 tokens, the cluster kernels spread d over at
 // most 8 CTAs, so each streams 0.5-1 MB of W_out through a ring while the
@@ -30,7 +30,6 @@ namespace narrow {
 constexpr int BM = 128;                       // tokens per tile (TMEM lanes)
 constexpr int BN = 64;                        // d columns per CTA (MMA N)
 constexpr int BK = 64;                        // K columns per X block / K rows per W box
-constexpr int KBLK = kMem / BK;               // 8
 constexpr int X_BLOCK_BYTES = BM * BK * 2;    // 16 KB: 128 rows x 128 B
 constexpr int W_BOX_BYTES = BK * BN * 2;      // 8 KB: 64 K-rows x 64 columns
 constexpr int H_BOX_BYTES = BM * BN * 2;      // 16 KB: 128 tokens x 64 columns
@@ -46,14 +45,22 @@ struct Shared {
     int abort;
 };
 
-constexpr int SMEM_BYTES = KBLK * X_BLOCK_BYTES + KBLK * W_BOX_BYTES + H_BOX_BYTES + (int)sizeof(Shared);
-static_assert(SMEM_BYTES <= 232448, "narrow projection shared memory over the per-CTA limit");
+// KBLK: 64-wide K-blocks of X (8: the concatenated [T,512] X; 4: one Engram
+// layer's [T,256] X).
+template <int KBLK>
+constexpr int smem_bytes() {
+    return KBLK * X_BLOCK_BYTES + KBLK * W_BOX_BYTES + H_BOX_BYTES + (int)sizeof(Shared);
+}
+static_assert(smem_bytes<kMem / BK>() <= 232448, "narrow projection shared memory over the per-CTA limit");
 
 struct Params {
-    const float *gate;  // [n_query], from the gather launch
+    const float *gate;  // [n_query], from the gather launch (GATED)
     int64_t n_query;
 };
 
+// GATED: h = bf16(h + gate * y), the concatenated form's token gate; without
+// it h = bf16(h + y) (one Engram layer, whose rows were gated before).
+template <int KBLK, bool GATED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     narrow_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap hl_map, const __grid_constant__ CUtensorMap hs_map,
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = q * 32 + lane;  // token row within the tile
         const int64_t t = m0 + row;
         grid_dependency_wait();  // the gates come from the gather launch
-        const float gate = t < p.n_query ? p.gate[t] : 0.f;
+        const float gate = GATED && t < p.n_query ? p.gate[t] : 0.f;
         if (mbar_wait(&sh->acc_full, 0, abort) && mbar_wait(&sh->wh_full, 0, abort)) {
             tc_fence_after();
             const uint32_t rbase = smem_u32(h_smem) + row * 128;
@@ -157,7 +164,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < 4; ++k) {
                         const float y0 = __uint_as_float(y[8 * k4 + 2 * k]);
                         const float y1 = __uint_as_float(y[8 * k4 + 2 * k + 1]);
-                        w[k] = pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])));
+                        w[k] = GATED ? pack_bf16x2(fmaf(gate, y0, bf16_lo(w[k])), fmaf(gate, y1, bf16_hi(w[k])))
+                                     : pack_bf16x2(bf16_lo(w[k]) + y0, bf16_hi(w[k]) + y1);
                     }
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
                                  "r"(w[2]), "r"(w[3])
