@@ -68,6 +68,31 @@ __device__ __forceinline__ int64_t hash_one(const HashParams &a, uint64_t seed, 
     return (int64_t)(a.pow2 ? (h & a.rmask) : (h % a.R));
 }
 
+// Row indices of tables j (module 0) and j + 24 (module 1): the same n-gram,
+// loaded once, through two seeds.
+__device__ __forceinline__ void hash_two(const HashParams &a, uint64_t seed0, uint64_t seed1, int j, int64_t start,
+                                         int64_t p, bool &bad, int64_t &r0, int64_t &r1) {
+    const int n = 2 + (j % kTablesPerModule) / 8;
+    uint64_t h0 = seed0, h1 = seed1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i < n) {
+            const int64_t q = p - (n - 1) + i;
+            int32_t id = a.V;
+            if (q >= start) {
+                id = __ldg(a.tokens + q);
+                if (id < 0 || id >= a.V) bad = true;
+            }
+            h0 = (h0 ^ (uint64_t)(uint32_t)id) * kGolden;
+            h0 ^= h0 >> 29;
+            h1 = (h1 ^ (uint64_t)(uint32_t)id) * kGolden;
+            h1 ^= h1 >> 29;
+        }
+    }
+    r0 = (int64_t)(a.pow2 ? (h0 & a.rmask) : (h0 % a.R));
+    r1 = (int64_t)(a.pow2 ? (h1 & a.rmask) : (h1 % a.R));
+}
+
 // Sequence s with offs[s] <= p < offs[s+1] (last such s; empty sequences skip).
 __device__ __forceinline__ int64_t find_seq(const int64_t *offs, int64_t n_seqs, int64_t p) {
     int64_t lo = 0, hi = n_seqs;
@@ -117,11 +142,16 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
 }
 
 // ============================================================ gather-reduce ==
-// One warp per (query token, module).  Lane l reads 16 bytes of row
-// (2i + l/16) at byte offset 16*(l%16) for i = 0..11: each warp-wide load
-// covers two whole 256-byte rows and all 12 loads are issued before the
-// arithmetic, so a warp keeps 6 KB of random reads in flight.  The two
-// half-warps' partial sums are merged with one xor-16 shuffle.
+// One warp per query token, its two modules in turn.  Lanes 0..23 find the
+// rows of both modules first (the n-gram ids are loaded once and hashed with
+// both modules' seeds), so a token's address chain is paid once.  Then, per
+// module, lane l reads 16 bytes of row (2i + l/16) at byte offset 16*(l%16)
+// for i = 0..11: each warp-wide load covers two whole 256-byte rows and all
+// 12 loads are issued before the arithmetic, so a warp keeps 6 KB of random
+// reads in flight.  The two half-warps' partial sums are merged with one
+// xor-16 shuffle.  (A warp per (token, module) paid the address chain twice:
+// 0.428 against 0.419 ms on the large workload, 0.701 against 0.610 ms on
+// prefill, whose repeated rows hit L2.)
 //
 // Row addresses come from an int64 idx array (HBM tables), an int32 slot
 // array (staged rows), or are hashed in-register by lanes 0..23 (the fused
@@ -231,91 +261,103 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
         __syncthreads();
     }
     const int lane = threadIdx.x & 31;
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t t = gw >> 1;
-    const int m = (int)(gw & 1);
+    const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // a warp per query token
     if (t >= P.n_query) return;
 
-    // lanes 0..23: this module's 24 row offsets and fp32 scales
-    int64_t off = 0;
-    float sc = 0.f;
-    int ok = 0;
+    // lanes 0..23: the 24 row offsets and fp32 scales of each module
+    int64_t offm[2] = {0, 0};
+    float scm[2] = {0.f, 0.f};
+    int okm[2] = {0, 0};
     if (lane < kTablesPerModule) {
-        const int j = kTablesPerModule * m + lane;
-        int64_t r;
+        int64_t rr[2];
         if (kHashed) {
             int64_t start, p;
             bool bad = !query_position(P.hp, t, start, p);
-            r = bad ? -1 : hash_one(P.hp, s_seed[j], j, start, p, bad);
-            if (bad) r = -1;
-        } else if (kMode == IDX_I64) {
-            r = __ldg(static_cast<const int64_t *>(P.idx) + t * kTables + j);
-        } else {
-            r = (int64_t)__ldg(static_cast<const int32_t *>(P.idx) + t * kTables + j);
+            if (!bad) hash_two(P.hp, s_seed[lane], s_seed[kTablesPerModule + lane], lane, start, p, bad, rr[0], rr[1]);
+            if (bad) rr[0] = rr[1] = -1;
         }
-        ok = (r >= 0 && r < P.R);
-        // a staged query with no slot (kSlotNone: the dedup overflowed or its
-        // index was out of range, both flagged there) contributes nothing
-        if (!ok && !(kMode == IDX_STAGED_I32 && r == kSlotNone)) raise_error(ENGRAM_ERANGE);
-        int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
-        if (kMode == IDX_HASH_SHARD && ok) {  // another shard's row adds nothing here
-            const int64_t k = r / P.n_shards;
-            ok = (r - k * P.n_shards) == P.shard;
-            flat = (int64_t)j * P.shard_rows + k;
-        }
-        if (ok) {
-            off = flat * P.row_stride;
-            if (!kMx)
-                sc = P.scales ? __ldg(P.scales + flat)
-                              : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int j = kTablesPerModule * m + lane;
+            int64_t r;
+            if (kHashed) {
+                r = rr[m];
+            } else if (kMode == IDX_I64) {
+                r = __ldg(static_cast<const int64_t *>(P.idx) + t * kTables + j);
+            } else {
+                r = (int64_t)__ldg(static_cast<const int32_t *>(P.idx) + t * kTables + j);
+            }
+            int ok = (r >= 0 && r < P.R);
+            // a staged query with no slot (kSlotNone: the dedup overflowed or its
+            // index was out of range, both flagged there) contributes nothing
+            if (!ok && !(kMode == IDX_STAGED_I32 && r == kSlotNone)) raise_error(ENGRAM_ERANGE);
+            int64_t flat = (kMode == IDX_STAGED_I32) ? r : (int64_t)j * P.R + r;
+            if (kMode == IDX_HASH_SHARD && ok) {  // another shard's row adds nothing here
+                const int64_t k = r / P.n_shards;
+                ok = (r - k * P.n_shards) == P.shard;
+                flat = (int64_t)j * P.shard_rows + k;
+            }
+            okm[m] = ok;
+            if (ok) {
+                offm[m] = flat * P.row_stride;
+                if (!kMx)
+                    scm[m] = P.scales ? __ldg(P.scales + flat)
+                                      : __ldg(reinterpret_cast<const float *>(P.rows + offm[m] + kRowBytes));
+            }
         }
     }
     const int half = lane >> 4;
     const int c16 = lane & 15;
-    uint4 v[12];
-    float s[12];
-    uint32_t sb[12];  // kMx: the E8M0 byte of the block holding this lane's 16 codes (block c16/2)
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m) {
+        const int64_t off = m ? offm[1] : offm[0];
+        const float sc = m ? scm[1] : scm[0];
+        const int ok = m ? okm[1] : okm[0];
+        uint4 v[12];
+        float s[12];
+        uint32_t sb[12];  // kMx: the E8M0 byte of the block holding this lane's 16 codes (block c16/2)
 #pragma unroll
-    for (int i = 0; i < 12; ++i) {
-        const int src = 2 * i + half;
-        const int64_t o = __shfl_sync(0xffffffffu, off, src);
-        if (!kMx) s[i] = __shfl_sync(0xffffffffu, sc, src);
-        if (kMx) sb[i] = __ldg(P.rows + o + kRowBytes + (c16 >> 1));
-        v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 ...
-        if (!__shfl_sync(0xffffffffu, ok, src)) {   // ... and is dropped (a finite scale times zero codes)
-            v[i] = make_uint4(0, 0, 0, 0);
-            if (kMx) sb[i] = 0;
+        for (int i = 0; i < 12; ++i) {
+            const int src = 2 * i + half;
+            const int64_t o = __shfl_sync(0xffffffffu, off, src);
+            if (!kMx) s[i] = __shfl_sync(0xffffffffu, sc, src);
+            if (kMx) sb[i] = __ldg(P.rows + o + kRowBytes + (c16 >> 1));
+            v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 ...
+            if (!__shfl_sync(0xffffffffu, ok, src)) {   // ... and is dropped (a finite scale times zero codes)
+                v[i] = make_uint4(0, 0, 0, 0);
+                if (kMx) sb[i] = 0;
+            }
         }
-    }
-    float acc[16];
+        float acc[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 12; ++i) {
-        if (kMx) s[i] = e8m0_to_float(sb[i]);
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        for (int i = 0; i < 12; ++i) {
+            if (kMx) s[i] = e8m0_to_float(sb[i]);
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 a = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
-            const float2 b = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
-            acc[4 * q + 0] = fmaf(s[i], a.x, acc[4 * q + 0]);
-            acc[4 * q + 1] = fmaf(s[i], a.y, acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(s[i], b.x, acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(s[i], b.y, acc[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) {
+                const float2 a = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
+                const float2 b = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
+                acc[4 * q + 0] = fmaf(s[i], a.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(s[i], a.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(s[i], b.x, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(s[i], b.y, acc[4 * q + 3]);
+            }
         }
-    }
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
-    const int64_t col = t * kMem + 256 * m + 16 * c16 + 8 * half;
-    const float *a = acc + 8 * half;
-    if (kBf16Out) {
-        uint16_t *dst = static_cast<uint16_t *>(P.out) + col;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                                                     pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
-    } else {
-        float *dst = static_cast<float *>(P.out) + col;
-        reinterpret_cast<float4 *>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
-        reinterpret_cast<float4 *>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+        for (int k = 0; k < 16; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 16);
+        const int64_t col = t * kMem + 256 * m + 16 * c16 + 8 * half;
+        const float *a = acc + 8 * half;
+        if (kBf16Out) {
+            uint16_t *dst = static_cast<uint16_t *>(P.out) + col;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                                         pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+        } else {
+            float *dst = static_cast<float *>(P.out) + col;
+            reinterpret_cast<float4 *>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
+            reinterpret_cast<float4 *>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+        }
     }
 }
 
@@ -859,7 +901,7 @@ engram_status gather_launch(int mode, bool bf16_out, const uint8_t *rows, const 
     P.R = R;
     P.out = out;
     if (hp) P.hp = *hp;
-    const int64_t warps = n_query * 2;
+    const int64_t warps = n_query;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
 #define ENGRAM_GATHER(M, B)                                         \
     do {                                                             \
@@ -1306,7 +1348,7 @@ static engram_status gather_gate_launch(const engram_config *cfg, const uint8_t 
     P.R = cfg->rows;
     P.out = X;
     P.hp = hp;
-    const int64_t gather_blocks = (n_query * 2 * 32 + 255) / 256;
+    const int64_t gather_blocks = (n_query * 32 + 255) / 256;
     const int64_t gate_blocks = (n_query * 32 + 255) / 256;
     P.gp.h = h;
     P.gp.g = g;
