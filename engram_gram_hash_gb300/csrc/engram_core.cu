@@ -261,7 +261,13 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
         __syncthreads();
     }
     const int lane = threadIdx.x & 31;
-    const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // a warp per query token
+    // A warp per query token; in the few-token form with gates a warp per
+    // (token, module), whose scale shuffles wait until its row loads are out:
+    // one memory round trip instead of three on the latency-bound path.
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t t = kGate ? wid >> 1 : wid;
+    const int m_first = kGate ? (int)(wid & 1) : 0;
+    const int m_last = kGate ? m_first : 1;
     if (t >= P.n_query) return;
 
     // lanes 0..23: the 24 row offsets and fp32 scales of each module
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
                 flat = (int64_t)j * P.shard_rows + k;
             }
             okm[m] = ok;
-            if (ok) {
+            if (ok && m >= m_first && m <= m_last) {
                 offm[m] = flat * P.row_stride;
                 if (!kMx)
                     scm[m] = P.scales ? __ldg(P.scales + flat)
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
     const int half = lane >> 4;
     const int c16 = lane & 15;
 #pragma unroll 1
-    for (int m = 0; m < 2; ++m) {
+    for (int m = m_first; m <= m_last; ++m) {
         const int64_t off = m ? offm[1] : offm[0];
         const float sc = m ? scm[1] : scm[0];
         const int ok = m ? okm[1] : okm[0];
@@ -320,13 +326,17 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
         for (int i = 0; i < 12; ++i) {
             const int src = 2 * i + half;
             const int64_t o = __shfl_sync(0xffffffffu, off, src);
-            if (!kMx) s[i] = __shfl_sync(0xffffffffu, sc, src);
+            if (!kMx && !kGate) s[i] = __shfl_sync(0xffffffffu, sc, src);
             if (kMx) sb[i] = __ldg(P.rows + o + kRowBytes + (c16 >> 1));
             v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 ...
             if (!__shfl_sync(0xffffffffu, ok, src)) {   // ... and is dropped (a finite scale times zero codes)
                 v[i] = make_uint4(0, 0, 0, 0);
                 if (kMx) sb[i] = 0;
             }
+        }
+        if (!kMx && kGate) {
+#pragma unroll
+            for (int i = 0; i < 12; ++i) s[i] = __shfl_sync(0xffffffffu, sc, 2 * i + half);
         }
         float acc[16];
 #pragma unroll
@@ -1348,8 +1358,8 @@ static engram_status gather_gate_launch(const engram_config *cfg, const uint8_t 
     P.R = cfg->rows;
     P.out = X;
     P.hp = hp;
-    const int64_t gather_blocks = (n_query * 32 + 255) / 256;
-    const int64_t gate_blocks = (n_query * 32 + 255) / 256;
+    const int64_t gather_blocks = (n_query * 64 + 255) / 256;  // a warp per (token, module)
+    const int64_t gate_blocks = (n_query * 32 + 255) / 256;    // a warp per token
     P.gp.h = h;
     P.gp.g = g;
     P.gp.gate = gate;
