@@ -440,9 +440,14 @@ def time_workload(eg, name, dev, steps, warmup):
     c = eg.make_config(cfg.V, cfg.R, cfg.d, default_seeds(), cfg.rms_eps)
     tok, offs = make_tokens(cfg)
     tokens, seq_offsets = torch.from_numpy(tok).to(dev), torch.from_numpy(offs).to(dev)
-    tables = torch.zeros((48, cfg.R, 256), dtype=torch.uint8, device=dev)
+    host = cfg.host_tables
+    if host:  # pinned host memory on huge pages, as the host-table line of run_ours
+        tables = eg.host_tables_empty((48, cfg.R, 256), torch.uint8)
+        scales = eg.host_tables_empty((48, cfg.R), torch.float32)
+    else:
+        tables = torch.zeros((48, cfg.R, 256), dtype=torch.uint8, device=dev)
+        scales = torch.empty((48, cfg.R), dtype=torch.float32, device=dev)
     sd.fill_tables(tables, cfg.seed)
-    scales = torch.empty((48, cfg.R), dtype=torch.float32, device=dev)
     sd.fill_scales(scales, cfg.seed)
     W = torch.empty((512, cfg.d), dtype=torch.bfloat16, device=dev)
     g = torch.empty(cfg.d, dtype=torch.bfloat16, device=dev)
@@ -451,11 +456,23 @@ def time_workload(eg, name, dev, steps, warmup):
     sd.fill_g(g, cfg.seed)
     sd.fill_h(h, cfg.seed)
     nq = cfg.tq
-    ws = torch.empty(eg.engram_forward_workspace_bytes(c, nq), dtype=torch.uint8, device=dev)
+    if host:
+        cap = nq * 48
+        ws = torch.empty(eg.engram_forward_host_workspace_bytes(c, nq, cap), dtype=torch.uint8, device=dev)
+        n_unique = torch.zeros(1, dtype=torch.int64, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        ev_a, ev_b = torch.cuda.Event(), torch.cuda.Event()
 
-    def fwd():
-        eg.engram_forward(c, tokens, seq_offsets, tables, scales, W, g, h, last_n=cfg.last_n, n_query=nq,
-                          workspace=ws)
+        def fwd():
+            eg.engram_forward_host(c, tokens, seq_offsets, tables, scales, W, g, h, cap, last_n=cfg.last_n,
+                                   n_query=nq, workspace=ws, n_unique=n_unique, side_stream=side, ev_dedup=ev_a,
+                                   ev_staged=ev_b)
+    else:
+        ws = torch.empty(eg.engram_forward_workspace_bytes(c, nq), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            eg.engram_forward(c, tokens, seq_offsets, tables, scales, W, g, h, last_n=cfg.last_n, n_query=nq,
+                              workspace=ws)
 
     for _ in range(warmup):
         fwd()
@@ -471,8 +488,14 @@ def time_workload(eg, name, dev, steps, warmup):
     ms = a.elapsed_time(b) / steps
     gbs = nominal_bytes_per_token(cfg.d) * nq / (ms * 1e-3) / 1e9
     res = {"workload": name, "query_tokens": nq, "R": cfg.R, "steps": steps, "ms_per_step": round(ms, 4),
-           "tokens_per_s": round(nq / (ms * 1e-3), 1), "step_roofline_frac": round(gbs / measured_peaks()["hbm_gbs"], 4)}
-    if nq <= 4096:
+           "tokens_per_s": round(nq / (ms * 1e-3), 1)}
+    if host:  # bound by the host link: the staging kernel against a pinned host-to-device copy
+        res["tables_in"] = "pinned host memory (huge pages)"
+        res["api"] = "engram_forward_host"
+        res["host_link_roofline"] = host_link_roofline(eg, c, cfg, tokens, seq_offsets, tables, scales, nq, dev)
+    else:
+        res["step_roofline_frac"] = round(gbs / measured_peaks()["hbm_gbs"], 4)
+    if nq <= 4096 and not host:
         res["cuda_graph"] = time_forward_graph(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
                                                max(steps, 200))
         w_out = 512 * cfg.d * 2
@@ -768,7 +791,15 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and args.also and not (args.rows or args.tokens or layers or sharded or host):
         del tables, scales
         torch.cuda.empty_cache()
-        out["also"] = [time_workload(eg, nm, dev, 20, 5) for nm in args.also.split(",") if nm and nm != args.workload]
+        out["also"] = []
+        for nm in args.also.split(","):
+            if not nm or nm == args.workload:
+                continue
+            try:
+                out["also"].append(time_workload(eg, nm, dev, 20, 5))
+            except Exception as e:  # an extra line never costs the main one
+                out["also"].append({"workload": nm, "error": f"{type(e).__name__}: {e}"[:300]})
+                torch.cuda.empty_cache()
     return out
 
 
@@ -1162,8 +1193,9 @@ def main():
                     help="host tables in engram_host_alloc memory (huge pages) or torch pinned memory")
     ap.add_argument("--host-chunks", type=int, nargs="*", default=[32768],
                     help="chunk sizes for the pipelined host-table path (host workload)")
-    ap.add_argument("--also", default="prefill,decode",
-                    help="other workloads timed after the main line (engram_forward, 20 steps), comma-separated")
+    ap.add_argument("--also", default="prefill,decode,host",
+                    help="other workloads timed after the main line (engram_forward, or engram_forward_host for host "
+                         "tables; 20 steps), comma-separated")
     ap.add_argument("--host-cache-slots", type=int, default=1 << 24,
                     help="rows of the HBM cache of staged rows timed beside the host-table path (0: skip)")
     ap.add_argument("--probe", action="store_true", help="print the random-row bandwidth ceilings and exit")
