@@ -186,33 +186,50 @@ struct GateParams {
 __device__ __forceinline__ void gate_pass(const GateParams &G, int64_t n_query, int64_t warp_id, int lane) {
     const int64_t t = warp_id;
     if (t >= n_query) return;
-    const uint16_t *hrow = G.h + t * G.d;
-    float ssum = 0.f, dsum = 0.f;
-    for (int r = 0; r < G.groups; ++r) {
-        const int col0 = r * G.cpg * fuse::BN;
-        float s = 0.f, d = 0.f;
-        for (int k = 0; k < G.cpg; ++k) {
-            const int ci = lane + 32 * k;  // 16-byte piece of the slice
-            const uint4 hv = __ldg(reinterpret_cast<const uint4 *>(hrow + col0) + ci);
-            const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(G.g + col0) + ci);
-            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    // Lane l's 16-byte piece i covers columns 8 (l + 32 i) .. +7; pieces
+    // r cpg .. (r + 1) cpg - 1 make up slice r.  The pieces are loaded in
+    // batches ahead of the arithmetic (one memory round trip per batch, not
+    // per piece), and summed in the same order as above.
+    const uint4 *hrow = reinterpret_cast<const uint4 *>(G.h + t * G.d);
+    const uint4 *grow = reinterpret_cast<const uint4 *>(G.g);
+    const int pieces = G.groups * G.cpg;
+    constexpr int kBatch = 8;
+    float ssum = 0.f, dsum = 0.f, s = 0.f, d = 0.f;
+    for (int i0 = 0; i0 < pieces; i0 += kBatch) {
+        uint4 hv[kBatch], gv[kBatch];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float a0 = bf16_lo(hw[e]), a1 = bf16_hi(hw[e]);
-                s = fmaf(a0, a0, s);
-                s = fmaf(a1, a1, s);
-                d = fmaf(a0, bf16_lo(gw[e]), d);
-                d = fmaf(a1, bf16_hi(gw[e]), d);
+        for (int b = 0; b < kBatch; ++b) {
+            if (i0 + b < pieces) {
+                hv[b] = __ldg(hrow + lane + 32 * (i0 + b));
+                gv[b] = __ldg(grow + lane + 32 * (i0 + b));
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            s += __shfl_xor_sync(0xffffffffu, s, o);
-            d += __shfl_xor_sync(0xffffffffu, d, o);
+        for (int b = 0; b < kBatch; ++b) {
+            const int i = i0 + b;
+            if (i < pieces) {
+                const uint32_t hw[4] = {hv[b].x, hv[b].y, hv[b].z, hv[b].w};
+                const uint32_t gw[4] = {gv[b].x, gv[b].y, gv[b].z, gv[b].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a0 = bf16_lo(hw[e]), a1 = bf16_hi(hw[e]);
+                    s = fmaf(a0, a0, s);
+                    s = fmaf(a1, a1, s);
+                    d = fmaf(a0, bf16_lo(gw[e]), d);
+                    d = fmaf(a1, bf16_hi(gw[e]), d);
+                }
+                if ((i + 1) % G.cpg == 0) {  // slice i / cpg complete: reduce over the warp, add in slice order
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        s += __shfl_xor_sync(0xffffffffu, s, o);
+                        d += __shfl_xor_sync(0xffffffffu, d, o);
+                    }
+                    ssum += s;
+                    dsum += d;
+                    s = d = 0.f;
+                }
+            }
         }
-        ssum += s;
-        dsum += d;
     }
     const float rinv = rsqrtf(ssum / (float)G.d + G.eps);
     const float gate = 1.f / (1.f + __expf(-(rinv * dsum * G.inv_sqrt_d)));

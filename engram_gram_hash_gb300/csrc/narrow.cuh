@@ -37,9 +37,11 @@ constexpr int TMEM_COLS = BN;                 // one fp32 accumulator
 constexpr int NUM_THREADS = 256;
 constexpr uint32_t IDESC = idesc_bf16(BM, BN, /*b_mn_major=*/true);
 
+constexpr int MAX_KBLK = kMem / BK;
+
 struct Shared {
-    uint64_t wh_full;  // W slice and h box landed
-    uint64_t x_full;   // X tile landed
+    uint64_t wh_full;             // W slice and h box landed
+    uint64_t x_full[MAX_KBLK];    // X K-block kb landed (the MMAs on it start at once)
     uint64_t acc_full;
     uint32_t tmem_base;
     int abort;
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&sh->wh_full, 1);
-        mbar_init(&sh->x_full, 1);
+        for (int kb = 0; kb < KBLK; ++kb) mbar_init(&sh->x_full[kb], 1);
         mbar_init(&sh->acc_full, 1);
         sh->abort = 0;
         fence_mbar_init();
@@ -108,20 +110,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_load_2d(w_smem + kb * W_BOX_BYTES, &w_map, &sh->wh_full, col0, kb * BK);
             tma_load_2d(h_smem, &hl_map, &sh->wh_full, col0, (int)m0);
             grid_dependency_wait();  // X is the gather's output
-            mbar_arrive_expect_tx(&sh->x_full, KBLK * X_BLOCK_BYTES);
-            for (int kb = 0; kb < KBLK; ++kb)
-                tma_load_2d(x_smem + kb * X_BLOCK_BYTES, &x_map, &sh->x_full, kb * BK, (int)m0);
+            for (int kb = 0; kb < KBLK; ++kb) {
+                mbar_arrive_expect_tx(&sh->x_full[kb], X_BLOCK_BYTES);
+                tma_load_2d(x_smem + kb * X_BLOCK_BYTES, &x_map, &sh->x_full[kb], kb * BK, (int)m0);
+            }
             // never leave with a copy still landing (also after an abort elsewhere)
             int no_abort = 0;
             mbar_wait(&sh->wh_full, 0, &no_abort, 200000000ull);
-            mbar_wait(&sh->x_full, 0, &no_abort, 200000000ull);
+            for (int kb = 0; kb < KBLK; ++kb) mbar_wait(&sh->x_full[kb], 0, &no_abort, 200000000ull);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            if (mbar_wait(&sh->wh_full, 0, abort) && mbar_wait(&sh->x_full, 0, abort)) {
-                tc_fence_after();
+            if (mbar_wait(&sh->wh_full, 0, abort)) {
                 const uint32_t xa = smem_u32(x_smem), wa = smem_u32(w_smem);
                 for (int kb = 0; kb < KBLK; ++kb) {
+                    if (!mbar_wait(&sh->x_full[kb], 0, abort)) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int s = 0; s < BK / 16; ++s) {
                         // A: X block kb, 32 bytes per K-step into each 128-byte swizzled row
@@ -143,7 +147,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int64_t t = m0 + row;
         grid_dependency_wait();  // the gates come from the gather launch
         const float gate = GATED && t < p.n_query ? p.gate[t] : 0.f;
-        if (mbar_wait(&sh->acc_full, 0, abort) && mbar_wait(&sh->wh_full, 0, abort)) {
+        // after a time-out elsewhere in the CTA the accumulator is incomplete: h is left as it was
+        if (mbar_wait(&sh->acc_full, 0, abort) && mbar_wait(&sh->wh_full, 0, abort) && !*abort) {
             tc_fence_after();
             const uint32_t rbase = smem_u32(h_smem) + row * 128;
 #pragma unroll
