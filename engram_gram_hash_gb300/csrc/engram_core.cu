@@ -1403,10 +1403,12 @@ static engram_status narrow_launch_t(const engram_config *cfg, const uint16_t *X
                                      uint16_t *h, int64_t n_query, cudaStream_t st) {
     const int d = cfg->d_model;
     const int k = KBLK * narrow::BK;
+    // a batch under one tile loads only its own rows (rounded up to a swizzle atom of 8)
+    const uint32_t box_rows = n_query < narrow::BM ? (uint32_t)((n_query + 7) / 8 * 8) : (uint32_t)narrow::BM;
     CUtensorMap wmap, xmap, hl, hs;
     if (!bf16_map_2d(&wmap, W, (uint64_t)d, (uint64_t)k, narrow::BN, narrow::BK) ||
-        !bf16_map_2d(&xmap, X, (uint64_t)k, (uint64_t)n_query, narrow::BK, narrow::BM) ||
-        !bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, narrow::BM) ||
+        !bf16_map_2d(&xmap, X, (uint64_t)k, (uint64_t)n_query, narrow::BK, box_rows) ||
+        !bf16_map_2d(&hl, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, box_rows) ||
         !bf16_map_2d(&hs, h, (uint64_t)d, (uint64_t)n_query, narrow::BN, 32))
         return cuda_fail(cudaErrorInvalidValue, "narrow projection tensor maps");
     static std::atomic<bool> attr_done[64] = {};
@@ -1417,6 +1419,7 @@ static engram_status narrow_launch_t(const engram_config *cfg, const uint16_t *X
     narrow::Params p;
     p.gate = gate;
     p.n_query = n_query;
+    p.box_rows = (int32_t)box_rows;
     cudaLaunchConfig_t lc = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -4,8 +4,9 @@
 // most 8 CTAs, so each streams 0.5-1 MB of W_out through a ring while the
 // other SMs idle.  Here every CTA owns one 64-column slice of d for one tile:
 // the whole grid is d/64 x tiles CTAs (64 at d = 4096), each loading its
-// W_out slice [512 x 64] (64 KB), the tile's X [128 x 512] (128 KB, from L2)
-// and its h box [128 x 64] in single TMA bursts, issuing 32 tcgen05 MMAs
+// W_out slice [512 x 64] (64 KB), the tile's X [128 x 512] (128 KB, from L2;
+// for a batch under 128 tokens only its own rows) and its h box [128 x 64]
+// in single TMA bursts, issuing 32 tcgen05 MMAs
 // (M = 128, N = 64, K = 16) into 64 TMEM columns, and applying
 // h = bf16(h + gate * y) to its box before one TMA store per warp.
 //
@@ -58,6 +59,8 @@ static_assert(smem_bytes<kMem / BK>() <= 232448, "narrow projection shared memor
 struct Params {
     const float *gate;  // [n_query], from the gather launch (GATED)
     int64_t n_query;
+    int32_t box_rows;   // token rows per X / h load box: the batch rounded up to 8, at most BM.  Rows past
+                        // it are not loaded; they only feed accumulator rows that are never stored.
 };
 
 // GATED: h = bf16(h + gate * y), the concatenated form's token gate; without
@@ -105,13 +108,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // not written by the gather: request before waiting for it
-            mbar_arrive_expect_tx(&sh->wh_full, KBLK * W_BOX_BYTES + H_BOX_BYTES);
+            const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;  // X K-block or h box: rows x 128 B
+            mbar_arrive_expect_tx(&sh->wh_full, KBLK * W_BOX_BYTES + box_bytes);
             for (int kb = 0; kb < KBLK; ++kb)
                 tma_load_2d(w_smem + kb * W_BOX_BYTES, &w_map, &sh->wh_full, col0, kb * BK);
             tma_load_2d(h_smem, &hl_map, &sh->wh_full, col0, (int)m0);
             grid_dependency_wait();  // X is the gather's output
             for (int kb = 0; kb < KBLK; ++kb) {
-                mbar_arrive_expect_tx(&sh->x_full[kb], X_BLOCK_BYTES);
+                mbar_arrive_expect_tx(&sh->x_full[kb], box_bytes);
                 tma_load_2d(x_smem + kb * X_BLOCK_BYTES, &x_map, &sh->x_full[kb], kb * BK, (int)m0);
             }
             // never leave with a copy still landing (also after an abort elsewhere)
