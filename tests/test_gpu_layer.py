@@ -29,6 +29,8 @@ CASES = {
     "d512_ragged": CONFIGS["tiny"].with_(d=512, seq_lens=(333, 2, 100), seed=7),
     "prefill_small": CONFIGS["prefill"].with_(seq_lens=(640, 421), R=1 << 16, seed=6),
     "decode_small": CONFIGS["decode"].with_(R=1 << 16),
+    # 37 queries: the d-split projection's load boxes round up to 40 rows
+    "decode_ragged": CONFIGS["decode"].with_(R=1 << 16, seq_lens=tuple(1 + (i % 4) for i in range(37)), seed=11),
 }
 
 

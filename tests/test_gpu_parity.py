@@ -31,6 +31,9 @@ SMALL = {
     "prefill_small": CONFIGS["prefill"].with_(seq_lens=(640, 421), R=1 << 16, seed=6),
     # decode: 64 sequences of 4 tokens, only the last one queried
     "decode_small": CONFIGS["decode"].with_(R=1 << 16),
+    # 37 queries (the d-split projection's load boxes round up to 40 rows),
+    # sequences of 1 to 4 tokens, so the n-gram windows reach the pad
+    "decode_ragged": CONFIGS["decode"].with_(R=1 << 16, seq_lens=tuple(1 + (i % 4) for i in range(37)), seed=11),
     # d = 512 (two 256-column chunks)
     "d512": CONFIGS["tiny"].with_(d=512, seq_lens=(333,), seed=7),
 }
@@ -95,7 +98,7 @@ def test_forward_small(eg, name):
     check_h(h, ref_h)
 
 
-@pytest.mark.parametrize("name", ["tiny", "prefill_small", "decode_small"])
+@pytest.mark.parametrize("name", ["tiny", "prefill_small", "decode_small", "decode_ragged"])
 def test_split_halves_equal_forward(eg, name):
     """engram_gather_x then engram_fuse_x gives engram_forward's bits, and X
     is bf16 of the fp32 module sums of engram_gather_reduce."""
@@ -216,7 +219,7 @@ def test_many_tiles_forward(eg):
     check_h(h1[torch.from_numpy(q).cuda()], rh)
 
 
-@pytest.mark.parametrize("name", ["decode_small", "tiny"])
+@pytest.mark.parametrize("name", ["decode_small", "decode_ragged", "tiny"])
 def test_forward_in_cuda_graph(eg, name):
     """engram_forward captured once in a CUDA graph and replayed gives the bits
     of the same call launched eagerly (no host sync or allocation inside)."""
