@@ -731,6 +731,24 @@ def run_ours(args, rank, world, local_rank):
     if not host and not layers and nq <= 4096:  # decode-sized batches: launch latency matters
         cuda_graph = time_forward_graph(eg, c, cfg, nq, tokens, seq_offsets, tables, scales, W, g, h, dev,
                                         max(K, 200))
+    elif layers and nq <= 4096:  # the per-layer form's launches, replayed from a CUDA graph
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            step()
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        reps = max(K, 200)
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record()
+        for _ in range(reps):
+            gr.replay()
+        gb.record()
+        torch.cuda.synchronize()
+        if eg.engram_last_error() != 0:
+            raise RuntimeError("device error in the CUDA-graph timing")
+        cuda_graph = {"api": "engram_layer_forward x 2 (module 0, then module 1)",
+                      "graph_us_per_step": round(ga.elapsed_time(gb) / reps * 1e3, 2), "steps": reps}
 
     peaks = measured_peaks()
     # algorithmic bytes per token; a layer moves its 24 rows + scales and h once each way
