@@ -77,6 +77,10 @@ template <bool RMS, bool SPLIT, bool SPLITK = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     query_kernel(const __grid_constant__ CUtensorMap h_map, const __grid_constant__ CUtensorMap w_map,
                  const __grid_constant__ QParams p) {
+    // a kernel launched as a programmatic dependent of this one (the gated
+    // gather) may start once every CTA has begun; it reads this kernel's
+    // output only after its grid_dependency_wait
+    allow_dependent_launch();
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_u32(smem) & 1023u) != 0) {
         if (threadIdx.x == 0) raise_error(ENGRAM_EUNSUPPORTED);
@@ -301,6 +305,7 @@ template <bool RMS, bool SPLIT>
 __global__ void __launch_bounds__(256) query_reduce_kernel(const float *__restrict__ part,
                                                            const float *__restrict__ ss, int splits, int64_t n,
                                                            int32_t d, float eps, void *out) {
+    allow_dependent_launch();  // as in query_kernel
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n * (BN / 4)) return;
     const int64_t t = g / (BN / 4);
