@@ -1319,13 +1319,31 @@ static engram_status query_launch(const engram_config *cfg, const uint16_t *A, i
         p.out = part;
         p.ss_out = part + (size_t)splits * n_query * kLayerWidth;
         p.kb_per_split = K / layer::BK / splits;
-        const dim3 grid((unsigned)p.m_tiles, (unsigned)splits);
-        kern<<<grid, layer::NUM_THREADS, layer::SMEM_BYTES, st>>>(amap, bmap, p);
+        // few tiles: both launches are programmatic dependents of the kernel
+        // before them (each waits before its first global read), so their
+        // set-up overlaps the previous kernel's tail
+        cudaLaunchConfig_t lc = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.gridDim = dim3((unsigned)p.m_tiles, (unsigned)splits);
+        lc.blockDim = dim3(layer::NUM_THREADS);
+        lc.dynamicSmemBytes = layer::SMEM_BYTES;
+        lc.stream = st;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        cudaError_t le = cudaLaunchKernelEx(&lc, kern, amap, bmap, p);
+        if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(query, split K)");
         s = launch_status();
         if (s != ENGRAM_OK) return s;
         const int64_t threads = n_query * (kLayerWidth / 4);
-        layer::query_reduce_kernel<RMS, SPLIT><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-            part, p.ss_out, splits, n_query, K, cfg->rms_eps, out);
+        lc.gridDim = dim3((unsigned)((threads + 255) / 256));
+        lc.blockDim = dim3(256);
+        lc.dynamicSmemBytes = 0;
+        const float *ss = p.ss_out;
+        le = cudaLaunchKernelEx(&lc, layer::query_reduce_kernel<RMS, SPLIT>, (const float *)part, ss, splits, n_query,
+                                (int32_t)K, cfg->rms_eps, out);
+        if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(query reduce)");
         return launch_status();
     }
     static std::atomic<bool> attr_done[64] = {};

@@ -127,6 +127,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool issued[NSTAGE] = {};
             uint32_t issued_parity[NSTAGE] = {};
+            // A may be the previous kernel's output (launched as its
+            // programmatic dependent for few tiles): the kernel's only global
+            // reads are these loads
+            grid_dependency_wait();
             for (int64_t mt = blockIdx.x; mt < p.m_tiles && !*abort; mt += gridDim.x) {
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort)) break;
@@ -306,6 +310,7 @@ __global__ void __launch_bounds__(256) query_reduce_kernel(const float *__restri
                                                            const float *__restrict__ ss, int splits, int64_t n,
                                                            int32_t d, float eps, void *out) {
     allow_dependent_launch();  // as in query_kernel
+    grid_dependency_wait();    // the partial products are the previous kernel's output
     const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n * (BN / 4)) return;
     const int64_t t = g / (BN / 4);
