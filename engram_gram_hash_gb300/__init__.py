@@ -84,6 +84,7 @@ def lib():
         sig = {
             "engram_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "engram_last_error": ([], ctypes.c_int),
+            "engram_wait_selftest": ([ctypes.c_uint64, P], ctypes.c_int),
             "engram_hash": ([C, P, P, i64, i32, i64, P, P], ctypes.c_int),
             "engram_gather_reduce": ([C, P, P, P, i64, P, P], ctypes.c_int),
             "engram_fuse": ([C, P, P, P, P, i64, P], ctypes.c_int),
@@ -136,6 +137,13 @@ def engram_status_string(status):
 def engram_last_error():
     """Sticky device error word of the current device as a status (clears it)."""
     return int(lib().engram_last_error())
+
+
+def engram_wait_selftest(limit_ns, stream=None):
+    """Enqueue the device-side time-limit check: a bounded wait that nothing
+    satisfies runs out after limit_ns and sets ETIMEOUT (read it with
+    engram_last_error())."""
+    _check(lib().engram_wait_selftest(int(limit_ns), _stream(stream)), "engram_wait_selftest")
 
 
 def _ptr(t):

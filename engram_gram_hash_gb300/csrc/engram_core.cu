@@ -1500,6 +1500,28 @@ extern "C" engram_status engram_last_error(void) {
     return ENGRAM_OK;
 }
 
+// A bounded device wait that is meant to run out: one thread initialises an
+// mbarrier that nothing arrives on and waits for it, as the projection
+// kernels wait on theirs, with the caller's limit.  The wait gives up, sets
+// ENGRAM_ETIMEOUT in the sticky word and the kernel returns; nothing traps
+// and the device stays usable.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort = 0;
+        fence_mbar_init();
+        mbar_wait(&bar, 0, &abort, limit_ns);  // no arrival ever: runs out after limit_ns
+    }
+}
+
+extern "C" engram_status engram_wait_selftest(uint64_t limit_ns, void *stream) {
+    if (limit_ns == 0 || limit_ns > UINT64_C(10000000000)) return ENGRAM_EINVAL;
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns);
+    return launch_status();
+}
+
 extern "C" engram_status engram_hash(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
                                      int64_t n_seqs, int32_t last_n, int64_t n_query, int64_t *idx, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || n_query < 0 || n_seqs < 0 || last_n < 0) return ENGRAM_EINVAL;

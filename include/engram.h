@@ -99,6 +99,14 @@ const char *engram_status_string(engram_status st);
  * (ENGRAM_OK if clear) and clears it.  Synchronises the device. */
 engram_status engram_last_error(void);
 
+/* Health check of the device-side time limits (not part of the Engram read):
+ * enqueues one small kernel whose bounded wait on a barrier that nothing
+ * arrives on runs out after limit_ns nanoseconds of device time.  The kernel
+ * then sets ENGRAM_ETIMEOUT in the sticky word and returns, as any projection
+ * or pipeline wait of this library does when it gives up; the device stays
+ * usable.  limit_ns in [1, 10^10], else ENGRAM_EINVAL (nothing enqueued). */
+engram_status engram_wait_selftest(uint64_t limit_ns, void *stream);
+
 /*
  * Row addresses: steps 1-2 above.  Addresses depend on token ids only (no
  * table is read), so a whole prompt can be hashed before its forward pass

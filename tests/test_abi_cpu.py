@@ -166,3 +166,11 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt and "oracle.c" not in txt, f
+
+
+def test_wait_selftest_checks_its_limit_before_device_work(eg):
+    """engram_wait_selftest rejects a zero or over-long limit with EINVAL and
+    enqueues nothing (no GPU is touched here)."""
+    lib = eg.lib()
+    assert lib.engram_wait_selftest(0, None) == 1
+    assert lib.engram_wait_selftest(10**10 + 1, None) == 1
