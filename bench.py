@@ -824,6 +824,31 @@ def run_ours(args, rank, world, local_rank):
         if args.host_cache_slots > 0 and args.layout != "mx":
             out["cached"] = time_host_cached(eg, c, cfg, tables, scales, W, g, h, dev, args.host_cache_slots,
                                              max(3, min(K, 20)))
+        if scales is not None:  # the same call with the fp32 scale array held in HBM instead (rows only cross the link)
+            scales_dev = scales.to(dev)
+
+            def fwd_dev_scales():
+                eg.engram_forward_host(c, tokens, seq_offsets, tables, scales_dev, W, g, h, cap, last_n=cfg.last_n,
+                                       n_query=nq, workspace=fws, n_unique=n_unique, side_stream=side, ev_dedup=ev_a,
+                                       ev_staged=ev_b)
+
+            for _ in range(3):
+                fwd_dev_scales()
+            torch.cuda.synchronize()
+            da, db = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(3, min(K, 20))
+            da.record()
+            for _ in range(reps):
+                fwd_dev_scales()
+            db.record()
+            torch.cuda.synchronize()
+            if eg.engram_last_error() != 0:
+                raise RuntimeError("device error in the device-scales host-table timing")
+            dms = da.elapsed_time(db) / reps
+            out["scales_in_hbm"] = {"ms_per_step": round(dms, 4), "tokens_per_s": round(nq / (dms * 1e-3), 1),
+                                    "steps": reps, "note": "tables in pinned host memory, the fp32 scale array "
+                                    "(48 x R x 4 B) in HBM: the link carries rows only"}
+            del scales_dev
     if not args.no_e2e and not layers and not sharded:
         out["e2e"] = e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h, nq, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not layers and not sharded:
