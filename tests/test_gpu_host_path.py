@@ -117,6 +117,22 @@ def test_host_path_bit_identical_to_hbm_path(eg):
     check_h(h_host[torch.from_numpy(q).cuda()], ref_h)
 
 
+def test_host_tables_with_scales_in_hbm(eg):
+    """Host tables with the fp32 scale array in device memory (read through
+    its unified address): the same h bits as with pinned host scales."""
+    w = Workload(SMALL_HOST, host_tables=True)
+    cfg = w.cfg
+    side = torch.cuda.Stream()
+    h_pinned, h_dev = w.fresh_h(), w.fresh_h()
+    eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h_pinned,
+                           capacity=cfg.tq * 48, side_stream=side)
+    eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, w.tables, w.scales.cuda(), w.W, w.g, h_dev,
+                           capacity=cfg.tq * 48, side_stream=side)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_pinned.view(torch.int16), h_dev.view(torch.int16))
+
+
 def test_host_path_record_layout(eg):
     """Host tables as 272-byte records (scale inside the row): same h bits as
     the HBM path with separate scales."""
