@@ -1200,11 +1200,15 @@ static engram_status fuse3_launch_t(const CUtensorMap &wmap, const CUtensorMap &
                              p.m_tiles, attr_done, max_clusters, st, pdl, wmap, xmap, hl, hs, p);
 }
 
-// Few tiles (under one per two SMs): the h-resident kernel, with d split into
-// slices of 1 chunk if that fits a cluster of 8, else 2.  Returns its chunks
-// per CTA, or 0 to use the other kernels (many tiles, or d too wide).
+// One or two tiles: the h-resident kernel, with d split into slices of 1
+// chunk if that fits a cluster of 8, else 2.  Returns its chunks per CTA, or
+// 0 to use the other kernels (more tiles, or d too wide).  From 3 tiles on
+// fuse2 is as fast or faster at every size measured (d = 4096: 384 tokens
+// 20.0 against 22.4 us, 4,096 tokens 46 against 58 us, 8,192 tokens 87
+// against 102 us); `engram_forward` sends 1-2 tiles to the d-split kernel,
+// which takes this split for its gates.
 static int pick_cpg_h_resident(int64_t m_tiles, int n_chunks) {
-    if (m_tiles * 2 >= num_sms()) return 0;
+    if (m_tiles >= 3) return 0;
     if (n_chunks <= fuse::MAX_GROUPS) return 1;
     if (n_chunks % 2 == 0 && n_chunks / 2 <= fuse::MAX_GROUPS) return 2;
     return 0;
