@@ -1274,6 +1274,7 @@ static bool narrow_fits(int64_t m_tiles, int d);
 // One Engram layer's projection: h = bf16(h + X W_m), X [n][256] bf16,
 // W_m [256][d] (fuse2 with 4 K-blocks and no token gate; the d-split kernel
 // when the batch fits one wave of 64-column CTAs).
+static int query_splits(int64_t m_tiles, int k);
 static engram_status layer_projection_launch(const engram_config *cfg, const uint16_t *X, const uint16_t *W,
                                              uint16_t *h, int64_t n_query, cudaStream_t st) {
     const int d = cfg->d_model;
@@ -1296,7 +1297,9 @@ static engram_status layer_projection_launch(const engram_config *cfg, const uin
         return cuda_fail(cudaErrorInvalidValue, "layer X map");
     CUtensorMap hp;
     if (!bf16_map_2d(&hp, h, (uint64_t)d, (uint64_t)n_query, 64, 32)) return cuda_fail(cudaErrorInvalidValue, "h piece map");
-    return fuse_dispatch<FUSE_LAYER>(wmap, xmap, hp, p, st);
+    // a programmatic dependent of the gated gather in the same batch range
+    // (its producer waits for X; the update warps read only h before that)
+    return fuse_dispatch<FUSE_LAYER>(wmap, xmap, hp, p, st, query_splits(p.m_tiles, d) > 1);
 }
 
 // out = s * (A @ B) on tcgen05 (layer::query_kernel): A bf16 [n][K], B bf16
@@ -2043,8 +2046,9 @@ extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t 
     // at 128 registers gave 16; 1.970 against 1.997 ms per two-layer step)
     const unsigned blocks = (unsigned)((n_query * 32 + 127) / 128);
     {
-        // as a programmatic dependent only for few tiles (the decode-sized
-        // batches, whose chain of small launches it shortens); on the large
+        // as a programmatic dependent while the query products are split over
+        // K (up to a quarter as many tiles as SMs: decode and chunk-sized
+        // batches, whose chain of short launches it shortens); on the large
         // workload the early blocks cost more than they hide (two-layer step
         // 2.156 against 1.971 ms)
         cudaLaunchConfig_t lc = {};
@@ -2055,7 +2059,7 @@ extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t 
         lc.blockDim = dim3(128);
         lc.stream = st;
         lc.attrs = attr;
-        lc.numAttrs = narrow_fits(m_tiles, d) ? 1 : 0;
+        lc.numAttrs = query_splits(m_tiles, d) > 1 ? 1 : 0;
         const cudaError_t le = cudaLaunchKernelEx(&lc, gather_gated_kernel, P);
         if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(gather_gated)");
     }
