@@ -156,6 +156,14 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _need_rows(t, dtype, name):
+    """Tables or scales for the HBM-path gathers: device memory, or pinned
+    host memory read in place over unified addressing."""
+    if t is not None and not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    _need(t, dtype, name, cuda=False)
+
+
 def _need(t, dtype, name, cuda=True):
     if t is None and name in ("scales", "host_scales", "staged_scales"):
         return  # rows that carry their scales (ROWS_RECORD, ROWS_MX)
@@ -196,8 +204,8 @@ def engram_hash(cfg, tokens, seq_offsets, last_n=0, n_query=None, idx=None, stre
 
 def engram_gather_reduce(cfg, tables, scales, idx, mem=None, stream=None):
     """mem fp32 [n_query, 512] from tables uint8 [48, R, 256], scales fp32 [48, R]."""
-    _need(tables, torch.uint8, "tables")
-    _need(scales, torch.float32, "scales")
+    _need_rows(tables, torch.uint8, "tables")
+    _need_rows(scales, torch.float32, "scales")
     _need(idx, torch.int64, "idx")
     nq = idx.shape[0]
     if mem is None:
@@ -233,8 +241,8 @@ def engram_forward(cfg, tokens, seq_offsets, tables, scales, W_out, g, h, last_n
     """Hash + gather + fuse in one call (HBM tables); h updated in place."""
     _need(tokens, torch.int32, "tokens")
     _need(seq_offsets, torch.int64, "seq_offsets")
-    _need(tables, torch.uint8, "tables")
-    _need(scales, torch.float32, "scales")
+    _need_rows(tables, torch.uint8, "tables")
+    _need_rows(scales, torch.float32, "scales")
     _need(W_out, torch.bfloat16, "W_out")
     _need(g, torch.bfloat16, "g")
     _need(h, torch.bfloat16, "h")
@@ -404,8 +412,8 @@ def engram_gather_x(cfg, tokens, seq_offsets, tables, scales, last_n=0, n_query=
     """Hash in registers + gather + reduce: X bf16 [n_query, 512]."""
     _need(tokens, torch.int32, "tokens")
     _need(seq_offsets, torch.int64, "seq_offsets")
-    _need(tables, torch.uint8, "tables")
-    _need(scales, torch.float32, "scales")
+    _need_rows(tables, torch.uint8, "tables")
+    _need_rows(scales, torch.float32, "scales")
     nq = _n_query(tokens, seq_offsets, last_n, n_query)
     if X is None:
         X = torch.empty((nq, MEM_DIM), dtype=torch.bfloat16, device=tokens.device)

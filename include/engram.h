@@ -153,6 +153,16 @@ engram_status engram_fuse(const engram_config *cfg, const float *mem, const uint
  * the projection, which loads X by TMA.  workspace >=
  * engram_forward_workspace_bytes(cfg, n_query) bytes of device memory,
  * 256-byte aligned (it holds X); its contents are scratch.
+ *
+ * tables (and scales) may also be pinned host memory, registered with CUDA
+ * (engram_host_alloc, cudaHostAlloc): the gather then reads each row in
+ * place over unified addressing ("vLLM reads pinned tables over UVA" in
+ * "Engram: the table that is never multiplied"), with the same results.  For
+ * decode-sized batches this beats engram_forward_host, whose dedup and
+ * staging carry a fixed cost (64 queries: 16.8 against 113 us per call;
+ * 512: 48 against 143 us; with scales in HBM and 51.5 GB of host tables);
+ * from a few thousand queries staging wins (4,096: 3.4 against 1.2 ms).
+ * The same holds for engram_gather_x and engram_gather_reduce.
  */
 size_t engram_forward_workspace_bytes(const engram_config *cfg, int64_t n_query);
 engram_status engram_forward(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,

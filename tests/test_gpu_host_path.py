@@ -133,6 +133,25 @@ def test_host_tables_with_scales_in_hbm(eg):
     assert torch.equal(h_pinned.view(torch.int16), h_dev.view(torch.int16))
 
 
+@pytest.mark.parametrize("cfg", [CONFIGS["decode"].with_(R=1 << 15, seed=12), SMALL_HOST],
+                         ids=["decode_64", "two_seqs_1255"])
+def test_forward_reads_pinned_host_tables_in_place(eg, cfg):
+    """engram_forward with the tables (and scales) in pinned host memory reads
+    the rows in place over unified addressing: the same h bits as with the
+    tables in HBM, scales pinned or in HBM."""
+    w = Workload(cfg, host_tables=True)
+    h_host, h_host_dsc, h_hbm = w.fresh_h(), w.fresh_h(), w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h_host, last_n=cfg.last_n)
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales.cuda(), w.W, w.g, h_host_dsc,
+                      last_n=cfg.last_n)
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables.cuda(), w.scales.cuda(), w.W, w.g, h_hbm,
+                      last_n=cfg.last_n)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_host.view(torch.int16), h_hbm.view(torch.int16))
+    assert torch.equal(h_host_dsc.view(torch.int16), h_hbm.view(torch.int16))
+
+
 def test_host_path_record_layout(eg):
     """Host tables as 272-byte records (scale inside the row): same h bits as
     the HBM path with separate scales."""
