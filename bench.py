@@ -1003,12 +1003,52 @@ def e2e_ours(args, eg, c, cfg, tokens, seq_offsets, tables, scales, W, g, h_dev,
     h2d = tok_h.numel() * 4 + off_h.numel() * 8 + h_in.numel() * 2
     d2h = h_out[0].numel() * 2
     api = "engram_forward_host" if cfg.host_tables else "engram_forward"
-    return {"value": round(rate, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / K, 4), "api": api,
-            "driving": "pipelined: copy in / forward / copy out on three streams, two buffer sets" if best
-            else "serial: copy in, forward, copy out on one stream",
-            "serial_ms_per_step": round(timed[False][1] / K, 4),
-            "pipelined_ms_per_step": round(timed[True][1] / K, 4)}
+    out = {"value": round(rate, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / K, 4), "api": api,
+           "driving": "pipelined: copy in / forward / copy out on three streams, two buffer sets" if best
+           else "serial: copy in, forward, copy out on one stream",
+           "serial_ms_per_step": round(timed[False][1] / K, 4),
+           "pipelined_ms_per_step": round(timed[True][1] / K, 4)}
+    out["link"] = link_rates(h_in, bufs[0][2], bufs[1][2], h_out[1], s_in, s_out)
+    if not cfg.host_tables:
+        # Pipelined steady state: each step's h crosses the link once each
+        # way while the other direction runs, so the duplex rate bounds it.
+        bound = max(h2d, d2h) / (out["link"]["duplex_GBps_per_direction"] * 1e9) * 1e3
+        out["link"]["pipelined_bound_ms_per_step"] = round(bound, 3)
+        out["link"]["pipelined_frac"] = round(bound / (timed[True][1] / K), 3)
+    return out
+
+
+def link_rates(h_in, d_a, d_b, h_back, s_in, s_out, reps=3):
+    """Pinned-host <-> device copy rates of the step's h, measured beside the
+    end-to-end steps with the same buffers and streams: host to device alone,
+    device to host alone, and both at once (the pipelined steps' case)."""
+    import torch
+
+    nbytes = h_in.numel() * h_in.element_size()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(to_dev, to_host, n):
+        torch.cuda.synchronize()
+        t0.record(s_in)
+        s_out.wait_event(t0)
+        for _ in range(n):
+            if to_dev:
+                with torch.cuda.stream(s_in):
+                    d_a.copy_(h_in, non_blocking=True)
+            if to_host:
+                with torch.cuda.stream(s_out):
+                    h_back.copy_(d_b, non_blocking=True)
+        joined = torch.cuda.Event()
+        joined.record(s_out)
+        s_in.wait_event(joined)
+        t1.record(s_in)
+        torch.cuda.synchronize()
+        return round(n * nbytes / (t0.elapsed_time(t1) * 1e-3) / 1e9, 1)
+
+    timed(True, True, 1)
+    return {"bytes_each_way": int(nbytes), "h2d_GBps": timed(True, False, reps),
+            "d2h_GBps": timed(False, True, reps), "duplex_GBps_per_direction": timed(True, True, reps)}
 
 
 # --------------------------------------------------------- the CPU oracle ---
