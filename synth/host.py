@@ -92,8 +92,16 @@ def h_rows(seed, d, t_idx):
 
 
 def w_out(seed, d):
-    """W_out bf16 bits [512, d], N(0, 1/512)."""
-    return bf16_words(seed, STREAM_W, W_SIGMA, 0, 512 * d).reshape(512, d)
+    """W_out bf16 bits [512, d], N(0, 1/512).  Drawn once per (seed, d) (a
+    512 x 32768 matrix takes ~20 s to draw); each call gets its own copy."""
+    return _w_out(int(seed), int(d)).copy()
+
+
+@functools.lru_cache(maxsize=4)
+def _w_out(seed, d):
+    w = bf16_words(seed, STREAM_W, W_SIGMA, 0, 512 * d).reshape(512, d)
+    w.setflags(write=False)
+    return w
 
 
 def layer_weights(seed, d, m):

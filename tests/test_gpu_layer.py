@@ -31,6 +31,9 @@ CASES = {
     "decode_small": CONFIGS["decode"].with_(R=1 << 16),
     # 37 queries: the d-split projection's load boxes round up to 40 rows
     "decode_ragged": CONFIGS["decode"].with_(R=1 << 16, seq_lens=tuple(1 + (i % 4) for i in range(37)), seed=11),
+    # d = 7168: 28 chunks (projection clusters of 7), query K = 7168
+    "d7168": CONFIGS["tiny"].with_(d=7168, seq_lens=(300, 29), seed=13),
+    "d7168_one_tile": CONFIGS["tiny"].with_(d=7168, seq_lens=(90,), seed=14),
 }
 
 

@@ -36,6 +36,16 @@ SMALL = {
     "decode_ragged": CONFIGS["decode"].with_(R=1 << 16, seq_lens=tuple(1 + (i % 4) for i in range(37)), seed=11),
     # d = 512 (two 256-column chunks)
     "d512": CONFIGS["tiny"].with_(d=512, seq_lens=(333,), seed=7),
+    # d = 1280: five chunks, so clusters of 5 CTAs of one chunk each; 9 tiles
+    # with a ragged tail (the forward pass takes the cluster kernel)
+    "d1280": CONFIGS["tiny"].with_(d=1280, seq_lens=(1000, 77), seed=12),
+    # d = 7168: 28 chunks, clusters of 7 CTAs of four chunks; 3 tiles
+    "d7168": CONFIGS["tiny"].with_(d=7168, seq_lens=(300, 29), seed=13),
+    # d = 7168 in one tile: the d-split projection on 112 CTAs, gates summed
+    # in the 7 x 4 chunk order
+    "d7168_one_tile": CONFIGS["tiny"].with_(d=7168, seq_lens=(90,), seed=14),
+    # the widest d the projection takes: clusters of 8 CTAs of 16 chunks
+    "d32768": CONFIGS["tiny"].with_(d=32768, seq_lens=(150,), seed=15),
 }
 
 
