@@ -85,7 +85,7 @@ typedef enum {
 
 typedef struct {
     int32_t vocab;       /* V: token ids must lie in [0, V); V itself is the pad id */
-    int32_t d_model;     /* d: residual width; engram_fuse needs d % 256 == 0 */
+    int32_t d_model;     /* d: residual width; the projection needs d % 256 == 0, 256 <= d <= 32768 */
     int64_t rows;        /* R: rows per table, R >= 1 */
     float rms_eps;       /* eps inside the rmsnorm of the gate (1e-6 by default) */
     uint32_t row_layout; /* ENGRAM_ROWS_SEPARATE, ENGRAM_ROWS_RECORD or ENGRAM_ROWS_MX */
@@ -142,7 +142,7 @@ engram_status engram_gather_reduce(const engram_config *cfg, const uint8_t *tabl
  *   W_out bf16 [512][d] row-major (16-byte aligned)
  *   g     bf16 [d]
  *   h     bf16 [n_query][d], read and updated in place (16-byte aligned)
- * Needs d % 256 == 0.
+ * Needs d % 256 == 0 and d <= 32768 (ENGRAM_EINVAL otherwise).
  */
 engram_status engram_fuse(const engram_config *cfg, const float *mem, const uint16_t *W_out, const uint16_t *g,
                           uint16_t *h, int64_t n_query, void *stream);

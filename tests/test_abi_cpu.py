@@ -80,6 +80,11 @@ def test_invalid_arguments_rejected_before_any_device_work(eg):
     c2 = eg.make_config(1024, 4096, 200, default_seeds())
     assert lib.engram_fuse(ctypes.byref(c2), ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
                            ctypes.c_void_p(256), 4, null) == 1
+    # d above the widest split (8 CTAs of 16 chunks of 256 columns), and d = 0
+    for d_bad in (32768 + 256, 0):
+        cw = eg.make_config(1024, 4096, d_bad, default_seeds())
+        assert lib.engram_fuse(ctypes.byref(cw), ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                               ctypes.c_void_p(256), 4, null) == 1, d_bad
     # R < 1
     c3 = eg.make_config(1024, 0, 256, default_seeds())
     assert lib.engram_gather_reduce(ctypes.byref(c3), ctypes.c_void_p(256), ctypes.c_void_p(256),
