@@ -179,3 +179,38 @@ def test_wait_selftest_checks_its_limit_before_device_work(eg):
     lib = eg.lib()
     assert lib.engram_wait_selftest(0, None) == 1
     assert lib.engram_wait_selftest(10**10 + 1, None) == 1
+
+
+def test_empty_batches_are_no_ops_before_device_work(eg):
+    """n_query = 0 returns ENGRAM_OK from every batch entry point, with null
+    buffers and without touching the device (this machine may have none)."""
+    lib = eg.lib()
+    from synth.configs import default_seeds
+
+    c = ctypes.byref(eg.make_config(1024, 4096, 4096, default_seeds()))
+    P, I64, I32, SZ, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_uint32
+    n, z = P(0), I64(0)
+    calls = {
+        "engram_hash": (c, n, n, I64(1), I32(0), z, n, n),
+        "engram_gather_reduce": (c, n, n, n, z, n, n),
+        "engram_fuse": (c, n, n, n, n, z, n),
+        "engram_fuse_x": (c, n, n, n, n, z, n),
+        "engram_forward": (c, n, n, I64(1), I32(0), z, n, n, n, n, n, n, SZ(0), n),
+        "engram_forward_no_workspace": (c, n, n, I64(1), I32(0), z, n, n, n, n, n, n),
+        "engram_gather_x": (c, n, n, I64(1), I32(0), z, n, n, n, n),
+        "engram_gather_reduce_shard": (c, I32(0), I32(2), n, n, I64(1), I32(0), z, n, n, n, n),
+        "engram_gather_reduce_staged": (c, n, n, n, z, I64(1), n, n),
+        "engram_layer_forward": (c, I32(1), n, n, I64(1), I32(0), z, n, n, n, n, n, n, n, SZ(0), n),
+        "engram_forward_host": (c, n, n, I64(1), I32(0), z, n, n, n, n, n, I64(1), n, SZ(0), n, n, n, n, n),
+        "engram_forward_host_pipelined": (c, n, n, I64(1), I32(0), z, n, n, n, n, n, I64(64), I64(1), n, SZ(0), n,
+                                          n, n, n),
+        "engram_forward_host_cached": (c, n, n, I64(1), I32(0), z, n, n, n, n, n, n, I64(1 << 10), I64(1 << 10),
+                                       U32(1), n, SZ(0), n, n, n, n, n),
+    }
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for name, args in calls.items():
+        decl = re.search(r"\b" + name + r"\s*\(([^;]*)\);", src)
+        assert decl and len(decl.group(1).split(",")) == len(args), name  # one value per declared parameter
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        assert f(*args) == 0, name
