@@ -304,6 +304,9 @@ engram_status engram_gather_reduce_staged(const engram_config *cfg, const uint8_
  * gather and fuse on `stream` after `ev_staged` (recorded on `side_stream`).
  * Both events are caller-created (cudaEventDisableTiming is fine).
  * workspace >= engram_forward_host_workspace_bytes(cfg, n_query, capacity).
+ * The call can be captured into a CUDA graph on `stream`: the side stream
+ * joins the capture through `ev_dedup` and rejoins `stream` through
+ * `ev_staged`; replays give the eager call's bits.
  */
 size_t engram_forward_host_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t capacity);
 engram_status engram_forward_host(const engram_config *cfg, const int32_t *tokens, const int64_t *seq_offsets,
@@ -424,7 +427,9 @@ engram_status engram_forward_host_cached(const engram_config *cfg, const int32_t
  * workspace >= engram_forward_host_pipelined_workspace_bytes(cfg, n_query,
  * chunk, capacity); host tables and scales as in engram_forward_host.
  * Argument errors return synchronously; device-side range and capacity errors
- * set the sticky error word.
+ * set the sticky error word.  Capturable into a CUDA graph on `stream` like
+ * engram_forward_host (every side-stream step waits on an event recorded in
+ * the same call).
  */
 size_t engram_forward_host_pipelined_workspace_bytes(const engram_config *cfg, int64_t n_query, int64_t chunk,
                                                      int64_t capacity);

@@ -283,3 +283,56 @@ def test_host_path_full_size(eg):
     check_h(h[torch.from_numpy(q).cuda()], ref_h)
     del w, h, idx
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("form", ["one_batch", "pipelined"])
+def test_host_path_in_cuda_graph(eg, form):
+    """The host-table path captured in a CUDA graph: the dedup on the main
+    stream, the staging on a side stream forked and joined by events, then
+    the staged gather and projection.  Each replay gives the bits of the same
+    call run eagerly (and a second replay applies the update again)."""
+    w = Workload(SMALL_HOST, host_tables=True)
+    cfg = w.cfg
+    nq, cap, chunk = cfg.tq, cfg.tq * 48, 512
+    dev = torch.device("cuda")
+    side, s = torch.cuda.Stream(), torch.cuda.Stream()
+    if form == "one_batch":
+        ws = torch.empty(eg.engram_forward_host_workspace_bytes(w.c, nq, cap), dtype=torch.uint8, device=dev)
+        nu = torch.zeros(1, dtype=torch.int64, device=dev)
+        evs = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def call(h):
+            return eg.engram_forward_host(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h,
+                                          capacity=cap, workspace=ws, n_unique=nu, stream=s, side_stream=side,
+                                          ev_dedup=evs[0], ev_staged=evs[1])
+    else:
+        ws = torch.empty(eg.engram_forward_host_pipelined_workspace_bytes(w.c, nq, chunk, chunk * 48),
+                         dtype=torch.uint8, device=dev)
+        nu = torch.zeros(-(-nq // chunk), dtype=torch.int64, device=dev)
+        evs = [torch.cuda.Event() for _ in range(6)]
+
+        def call(h):
+            return eg.engram_forward_host_pipelined(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h,
+                                                    chunk=chunk, workspace=ws, n_unique=nu, stream=s,
+                                                    side_stream=side, events=evs)
+
+    h_eager = w.fresh_h()
+    with torch.cuda.stream(s):
+        call(h_eager)
+        call(h_eager)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    nu_eager = nu.clone()
+
+    h_graph = w.fresh_h()
+    nu.zero_()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call(h_graph)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_graph.view(torch.int16), h_eager.view(torch.int16))
+    assert torch.equal(nu, nu_eager)
