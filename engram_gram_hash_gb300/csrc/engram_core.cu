@@ -1324,7 +1324,8 @@ static int query_splits(int64_t m_tiles, int k) {
 // query_reduce_kernel.
 template <bool RMS, bool SPLIT>
 static engram_status query_launch(const engram_config *cfg, const uint16_t *A, int K, const uint16_t *B, void *out,
-                                  int64_t n_query, cudaStream_t st, int splits = 1, float *part = nullptr) {
+                                  int64_t n_query, cudaStream_t st, int splits = 1, float *part = nullptr,
+                                  bool pdl = true) {
     layer::QParams p;
     memset(&p, 0, sizeof(p));
     p.out = out;
@@ -1345,9 +1346,10 @@ static engram_status query_launch(const engram_config *cfg, const uint16_t *A, i
         p.out = part;
         p.ss_out = part + (size_t)splits * n_query * kLayerWidth;
         p.kb_per_split = K / layer::BK / splits;
-        // few tiles: both launches are programmatic dependents of the kernel
-        // before them (each waits before its first global read), so their
-        // set-up overlaps the previous kernel's tail
+        // few tiles: the reduction is a programmatic dependent of the split
+        // products, and they of the kernel before them when pdl (each waits
+        // before its first global read), so their set-up overlaps the
+        // previous kernel's tail
         cudaLaunchConfig_t lc = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1357,7 +1359,7 @@ static engram_status query_launch(const engram_config *cfg, const uint16_t *A, i
         lc.dynamicSmemBytes = layer::SMEM_BYTES;
         lc.stream = st;
         lc.attrs = attr;
-        lc.numAttrs = 1;
+        lc.numAttrs = pdl ? 1 : 0;
         cudaError_t le = cudaLaunchKernelEx(&lc, kern, amap, bmap, p);
         if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(query, split K)");
         s = launch_status();
@@ -1366,6 +1368,7 @@ static engram_status query_launch(const engram_config *cfg, const uint16_t *A, i
         lc.gridDim = dim3((unsigned)((threads + 255) / 256));
         lc.blockDim = dim3(256);
         lc.dynamicSmemBytes = 0;
+        lc.numAttrs = 1;
         const float *ss = p.ss_out;
         le = cudaLaunchKernelEx(&lc, layer::query_reduce_kernel<RMS, SPLIT>, (const float *)part, ss, splits, n_query,
                                 (int32_t)K, cfg->rms_eps, out);
@@ -2025,7 +2028,14 @@ extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t 
     // (few tiles: K split over several CTAs per tile, partial products added up)
     const int64_t m_tiles = (n_query + layer::BM - 1) / layer::BM;
     float *part = reinterpret_cast<float *>(ws + layer_off_part(n_query));
-    engram_status s = query_launch<true, true>(cfg, h, d, W_q, qpair, n_query, st, query_splits(m_tiles, d), part);
+    // The layer's first kernel is an ordinary launch: it starts after all
+    // earlier work in the stream has finished, the previous layer's update of
+    // h included.  Every later kernel of the layer is a programmatic
+    // dependent of the one before it and may start early; the projection
+    // loads its h box before its dependency wait, which is safe only because
+    // nothing launched after this first kernel writes h before it.
+    engram_status s = query_launch<true, true>(cfg, h, d, W_q, qpair, n_query, st, query_splits(m_tiles, d), part,
+                                               /*pdl=*/false);
     if (s != ENGRAM_OK) return s;
     s = query_launch<false, false>(cfg, qpair, 2 * kLayerWidth, W_kk, u, n_query, st,
                                    query_splits(m_tiles, 2 * kLayerWidth), part);

@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     narrow_kernel(const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap hl_map, const __grid_constant__ CUtensorMap hs_map,
                   const __grid_constant__ Params p) {
-    // The next layer's first query kernel, launched as a programmatic
-    // dependent, waits for this grid before it reads h.
+    // A kernel launched after this one as a programmatic dependent may start
+    // once every CTA has begun; it must wait for this grid before it reads h.
     allow_dependent_launch();
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_u32(smem) & 1023u) != 0) {  // same for every CTA: all leave together

@@ -258,3 +258,42 @@ def test_layer_argument_errors(eg):
     assert ex.value.status == 7
     torch.cuda.synchronize()
     assert eg.engram_last_error() == 0
+
+
+@pytest.mark.parametrize("name", ["decode_ragged", "prefill_small"])
+def test_layers_in_cuda_graph(eg, name):
+    """Both layers captured in one CUDA graph (their split-K query kernels,
+    reductions and dependent launches included) give the eager bits."""
+    cfg = CASES[name]
+    w = Workload(cfg)
+    nq = cfg.tq
+    ws = torch.empty(eg.engram_layer_workspace_bytes(w.c, nq), dtype=torch.uint8, device="cuda")
+    mats = []
+    for m in (0, 1):
+        wq, wk, wm = _weights(eg, cfg, m)
+        mats.append((wq, eg.engram_layer_keys(w.c, wk), wm))
+    s = torch.cuda.Stream()
+
+    def step(h):
+        for m in (0, 1):
+            wq, wkk, wm = mats[m]
+            eg.engram_layer_forward(w.c, m, w.tokens, w.seq_offsets, w.tables, w.scales, wq, wkk, wm, h,
+                                    last_n=cfg.last_n, n_query=nq, workspace=ws, stream=s)
+
+    h_eager = w.fresh_h()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step(h_eager)
+        step(h_eager)
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    h_graph = w.fresh_h()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(h_graph)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h_graph.view(torch.int16), h_eager.view(torch.int16))
