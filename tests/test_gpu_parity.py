@@ -255,6 +255,34 @@ def test_forward_in_cuda_graph(eg, name):
     assert not torch.equal(h1.view(torch.int16), h2.view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["decode_small", "prefill_small", "d7168"])
+def test_dependent_forward_steps_in_one_graph(eg, name):
+    """Three engram_forward calls on the same h captured in one CUDA graph (each
+    step reads the h the previous one wrote, with no host launch gap between
+    them) give the bits of the same three calls made eagerly."""
+    w = Workload(SMALL[name])
+    nq = w.cfg.tq
+    ws = torch.empty(max(eg.engram_forward_workspace_bytes(w.c, nq), 1), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def steps(h):
+        for _ in range(3):
+            eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, last_n=w.cfg.last_n,
+                              n_query=nq, workspace=ws, stream=s)
+
+    h_eager, h_graph = w.fresh_h(), w.fresh_h()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        steps(h_eager)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        steps(h_graph)
+    graph.replay()
+    _clear(eg)
+    assert torch.equal(h_eager.view(torch.int16), h_graph.view(torch.int16))
+
+
 def test_generator_twin_rows_match_host(eg):
     """The device-filled tables/scales/h equal the host draws bit for bit."""
     cfg = SMALL["ragged_prime"]
