@@ -183,57 +183,62 @@ struct GateParams {
     float eps, inv_sqrt_d;
 };
 
-__device__ __forceinline__ void gate_pass(const GateParams &G, int64_t n_query, int64_t warp_id, int lane) {
-    const int64_t t = warp_id;
-    if (t >= n_query) return;
-    // Lane l's 16-byte piece i covers columns 8 (l + 32 i) .. +7; pieces
-    // r cpg .. (r + 1) cpg - 1 make up slice r.  The pieces are loaded in
-    // batches ahead of the arithmetic (one memory round trip per batch, not
-    // per piece), and summed in the same order as above.
-    const uint4 *hrow = reinterpret_cast<const uint4 *>(G.h + t * G.d);
-    const uint4 *grow = reinterpret_cast<const uint4 *>(G.g);
-    const int pieces = G.groups * G.cpg;
-    constexpr int kBatch = 8;
-    float ssum = 0.f, dsum = 0.f, s = 0.f, d = 0.f;
-    for (int i0 = 0; i0 < pieces; i0 += kBatch) {
-        uint4 hv[kBatch], gv[kBatch];
+// One block per query token: warp r (< groups) sums slice r, the slice's
+// pieces loaded together (one memory round trip), and thread 0 adds the
+// slices' sums in slice order.  The same additions in the same order as one
+// warp walking the slices in turn, with all slices' loads in flight at once.
+__device__ __forceinline__ void gate_block(const GateParams &G, int64_t n_query, int64_t t, int warp, int lane) {
+    __shared__ float2 slice_sum[fuse::MAX_GROUPS];
+    if (t < n_query && warp < G.groups) {
+        // Lane l's 16-byte piece i covers columns 8 (l + 32 i) .. +7; pieces
+        // r cpg .. (r + 1) cpg - 1 make up slice r.
+        const uint4 *hrow = reinterpret_cast<const uint4 *>(G.h + t * G.d);
+        const uint4 *grow = reinterpret_cast<const uint4 *>(G.g);
+        const int i_end = (warp + 1) * G.cpg;
+        constexpr int kBatch = 8;
+        float s = 0.f, d = 0.f;
+        for (int i0 = warp * G.cpg; i0 < i_end; i0 += kBatch) {
+            uint4 hv[kBatch], gv[kBatch];
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            if (i0 + b < pieces) {
-                hv[b] = __ldg(hrow + lane + 32 * (i0 + b));
-                gv[b] = __ldg(grow + lane + 32 * (i0 + b));
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int i = i0 + b;
-            if (i < pieces) {
-                const uint32_t hw[4] = {hv[b].x, hv[b].y, hv[b].z, hv[b].w};
-                const uint32_t gw[4] = {gv[b].x, gv[b].y, gv[b].z, gv[b].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a0 = bf16_lo(hw[e]), a1 = bf16_hi(hw[e]);
-                    s = fmaf(a0, a0, s);
-                    s = fmaf(a1, a1, s);
-                    d = fmaf(a0, bf16_lo(gw[e]), d);
-                    d = fmaf(a1, bf16_hi(gw[e]), d);
+            for (int b = 0; b < kBatch; ++b) {
+                if (i0 + b < i_end) {
+                    hv[b] = __ldg(hrow + lane + 32 * (i0 + b));
+                    gv[b] = __ldg(grow + lane + 32 * (i0 + b));
                 }
-                if ((i + 1) % G.cpg == 0) {  // slice i / cpg complete: reduce over the warp, add in slice order
+            }
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        s += __shfl_xor_sync(0xffffffffu, s, o);
-                        d += __shfl_xor_sync(0xffffffffu, d, o);
+            for (int b = 0; b < kBatch; ++b) {
+                if (i0 + b < i_end) {
+                    const uint32_t hw[4] = {hv[b].x, hv[b].y, hv[b].z, hv[b].w};
+                    const uint32_t gw[4] = {gv[b].x, gv[b].y, gv[b].z, gv[b].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = bf16_lo(hw[e]), a1 = bf16_hi(hw[e]);
+                        s = fmaf(a0, a0, s);
+                        s = fmaf(a1, a1, s);
+                        d = fmaf(a0, bf16_lo(gw[e]), d);
+                        d = fmaf(a1, bf16_hi(gw[e]), d);
                     }
-                    ssum += s;
-                    dsum += d;
-                    s = d = 0.f;
                 }
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+            d += __shfl_xor_sync(0xffffffffu, d, o);
+        }
+        if (lane == 0) slice_sum[warp] = make_float2(s, d);
     }
-    const float rinv = rsqrtf(ssum / (float)G.d + G.eps);
-    const float gate = 1.f / (1.f + __expf(-(rinv * dsum * G.inv_sqrt_d)));
-    if (lane == 0) G.gate[t] = gate;
+    __syncthreads();
+    if (threadIdx.x == 0 && t < n_query) {
+        float ssum = 0.f, dsum = 0.f;
+        for (int r = 0; r < G.groups; ++r) {
+            ssum += slice_sum[r].x;
+            dsum += slice_sum[r].y;
+        }
+        const float rinv = rsqrtf(ssum / (float)G.d + G.eps);
+        G.gate[t] = 1.f / (1.f + __expf(-(rinv * dsum * G.inv_sqrt_d)));
+    }
 }
 
 struct GatherParams {
@@ -265,9 +270,9 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
     // on what does not depend on X.
     allow_dependent_launch();
     if constexpr (kGate) {  // the blocks past the gather's compute token gates
-        if ((int64_t)blockIdx.x >= P.gp.gather_blocks) {
-            gate_pass(P.gp, P.n_query, ((int64_t)(blockIdx.x - P.gp.gather_blocks) * blockDim.x + threadIdx.x) >> 5,
-                      threadIdx.x & 31);
+        if ((int64_t)blockIdx.x >= P.gp.gather_blocks) {  // block-uniform
+            gate_block(P.gp, P.n_query, (int64_t)blockIdx.x - P.gp.gather_blocks, (int)(threadIdx.x >> 5),
+                       (int)(threadIdx.x & 31));
             return;
         }
     }
@@ -1414,7 +1419,7 @@ static bool fuse_split(int64_t m_tiles, int n_chunks, int *groups, int *cpg) {
     return *cpg <= 16;
 }
 
-// Hash + gather -> bf16 X, plus one warp per query token computing its gate
+// Hash + gather -> bf16 X, plus one block per query token computing its gate
 // in fuse_split's order (extra blocks of the same launch).
 static engram_status gather_gate_launch(const engram_config *cfg, const uint8_t *tables, const float *scales,
                                         const HashParams &hp, int64_t n_query, uint16_t *X, const uint16_t *h,
@@ -1429,7 +1434,7 @@ static engram_status gather_gate_launch(const engram_config *cfg, const uint8_t 
     P.out = X;
     P.hp = hp;
     const int64_t gather_blocks = (n_query * 64 + 255) / 256;  // a warp per (token, module)
-    const int64_t gate_blocks = (n_query * 32 + 255) / 256;    // a warp per token
+    const int64_t gate_blocks = n_query;                       // a block per token, a warp per slice of d
     P.gp.h = h;
     P.gp.g = g;
     P.gp.gate = gate;

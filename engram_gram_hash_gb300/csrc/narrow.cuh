@@ -11,7 +11,7 @@
 // h = bf16(h + gate * y) to its box before one TMA store per warp.
 //
 // The token gate needs the whole h row, which no CTA holds here: it comes
-// precomputed (gate_pass in engram_core.cu, run by extra warps of the gather
+// precomputed (gate_block in engram_core.cu, run by extra blocks of the gather
 // launch) with the cluster kernels' reduction order, so the result has their
 // bits.  The kernel is launched as a programmatic dependent of that gather:
 // W_out and h, which the gather does not write, are requested before

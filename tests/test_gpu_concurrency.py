@@ -86,7 +86,8 @@ def test_streams_run_concurrently_with_serial_bits(eg):
 
     # and the first of the REPS calls against the oracle, on a fresh h
     for k, w in ws.items():
-        h1 = w.fresh_h()
+        h1 = w.fresh_h()  # filled on the current stream: finish before another stream reads it
+        torch.cuda.synchronize()
         _forward(eg, w, h1, work[k], streams[(k, "f")])
         torch.cuda.synchronize()
         _, _, _, ref_h, _ = w.ref_for(np.arange(w.cfg.tq))

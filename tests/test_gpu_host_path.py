@@ -317,6 +317,7 @@ def test_host_path_in_cuda_graph(eg, form):
                                                     side_stream=side, events=evs)
 
     h_eager = w.fresh_h()
+    torch.cuda.synchronize()  # h is filled on the current stream
     with torch.cuda.stream(s):
         call(h_eager)
         call(h_eager)
