@@ -68,6 +68,8 @@ def _load():
         lib.orc_fuse.argtypes = [P, P, P, P, i64, i32, ctypes.c_double, P]
         lib.orc_layer_gated.restype = ctypes.c_int
         lib.orc_layer_gated.argtypes = [P, P, P, P, P, P, i64, i32, ctypes.c_double, P, P]
+        lib.orc_layer_gated_mx.restype = ctypes.c_int
+        lib.orc_layer_gated_mx.argtypes = [P, P, P, P, P, P, i64, i32, ctypes.c_double, P, P]
         _lib = lib
     return _lib
 
@@ -189,19 +191,21 @@ def layer_gated(codes, scales, Wq, Wk, Wm, h, eps=1e-6):
     returns (h_new uint16 [T,d], gates float64 [T,24], e float64 [T,256]).
 
     codes uint8 [T,24,256] and scales float32 [T,24] are the layer's 24 rows
-    per token; Wq [d,256], Wk [256,256], Wm [256,d] and h [T,d] are bf16 bit
+    per token (MXFP8-style rows: scales uint8 [T,24,8], the E8M0 scale of each
+    32-code block); Wq [d,256], Wk [256,256], Wm [256,d] and h [T,d] are bf16 bit
     patterns (h is not modified; a copy is updated)."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
-    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    mx = np.asarray(scales).dtype == np.uint8
+    scales = np.ascontiguousarray(scales, dtype=np.uint8 if mx else np.float32)
     Wq = np.ascontiguousarray(Wq, dtype=np.uint16)
     Wk = np.ascontiguousarray(Wk, dtype=np.uint16)
     Wm = np.ascontiguousarray(Wm, dtype=np.uint16)
     hn = np.array(h, dtype=np.uint16, copy=True, order="C")
     T, d = hn.shape
-    assert codes.shape == (T, 24, ROW) and scales.shape == (T, 24)
+    assert codes.shape == (T, 24, ROW) and scales.shape == ((T, 24, 8) if mx else (T, 24))
     assert Wq.shape == (d, ROW) and Wk.shape == (ROW, ROW) and Wm.shape == (ROW, d)
     gates = np.zeros((T, 24), dtype=np.float64)
     e = np.zeros((T, ROW), dtype=np.float64)
-    _check(_load().orc_layer_gated(_p(codes), _p(scales), _p(Wq), _p(Wk), _p(Wm), _p(hn), T, d, eps, _p(gates),
-                                   _p(e)))
+    f = _load().orc_layer_gated_mx if mx else _load().orc_layer_gated
+    _check(f(_p(codes), _p(scales), _p(Wq), _p(Wk), _p(Wm), _p(hn), T, d, eps, _p(gates), _p(e)))
     return hn, gates, e

@@ -293,10 +293,28 @@ int orc_fuse(const double *mem, const uint16_t *W, const uint16_t *g, uint16_t *
  *
  * codes: e4m3 [T][24][256]; scales: fp32 [T][24]; h: bf16 [T][d], updated in
  * place; gates (optional): [T][24] out; e_out (optional): [T][256] out.
+ * With MXFP8-style rows (orc_layer_gated_mx) r_j's code c is scaled by the
+ * E8M0 scale of its 32-code block instead, escales [T][24][8].
  */
+static int layer_gated(const uint8_t *codes, const float *scales, const uint8_t *escales, const uint16_t *Wq,
+                       const uint16_t *Wk, const uint16_t *Wm, uint16_t *h, int64_t T, int32_t d, double eps,
+                       double *gates, double *e_out);
+
 int orc_layer_gated(const uint8_t *codes, const float *scales, const uint16_t *Wq, const uint16_t *Wk,
                     const uint16_t *Wm, uint16_t *h, int64_t T, int32_t d, double eps, double *gates,
                     double *e_out) {
+    return layer_gated(codes, scales, NULL, Wq, Wk, Wm, h, T, d, eps, gates, e_out);
+}
+
+int orc_layer_gated_mx(const uint8_t *codes, const uint8_t *escales, const uint16_t *Wq, const uint16_t *Wk,
+                       const uint16_t *Wm, uint16_t *h, int64_t T, int32_t d, double eps, double *gates,
+                       double *e_out) {
+    return layer_gated(codes, NULL, escales, Wq, Wk, Wm, h, T, d, eps, gates, e_out);
+}
+
+static int layer_gated(const uint8_t *codes, const float *scales, const uint8_t *escales, const uint16_t *Wq,
+                       const uint16_t *Wk, const uint16_t *Wm, uint16_t *h, int64_t T, int32_t d, double eps,
+                       double *gates, double *e_out) {
     enum { R = 256, J = 24 };
     if (d <= 0) return ORC_EINVAL;
     double *q = (double *)malloc(sizeof(double) * R);
@@ -323,9 +341,9 @@ int orc_layer_gated(const uint8_t *codes, const float *scales, const uint16_t *W
         for (int c = 0; c < R; ++c) e[c] = 0.0;
         for (int j = 0; j < J; ++j) {
             const uint8_t *row = codes + (t * J + j) * R;
-            const double s = (double)scales[t * J + j];
             double vs = 0.0;
             for (int c = 0; c < R; ++c) {
+                const double s = escales ? orc_e8m0_value(escales[(t * J + j) * 8 + c / 32]) : (double)scales[t * J + j];
                 v[c] = s * orc_e4m3_value(row[c]);
                 vs += v[c] * v[c];
             }

@@ -575,6 +575,44 @@ def test_layer_gate_symmetries():
     assert np.allclose(e4 - e1, g1[:, 7:8] * r7, rtol=1e-12, atol=1e-12)
 
 
+def test_layer_mx_equal_block_scales_match_one_row_scale():
+    """MXFP8-style rows whose eight E8M0 bytes all equal E give exactly the
+    one-scale form with scale 2^(E - 127) (the same doubles: a power of two
+    times an e4m3 value), for h, gates and e."""
+    codes, _, Wq, Wk, Wm, h = _layer_inputs(T=3, d=512, seed=43)
+    E = np.random.default_rng(9).integers(124, 131, (3, 24)).astype(np.uint8)
+    esc = np.repeat(E[:, :, None], 8, axis=2)
+    want = oracle.layer_gated(codes, np.ldexp(1.0, E.astype(np.int32) - 127).astype(np.float32), Wq, Wk, Wm, h)
+    got = oracle.layer_gated(codes, esc, Wq, Wk, Wm, h)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+
+
+def test_layer_mx_block_scale_applies_to_its_32_codes():
+    """Block b's scale byte 128 (x2) against byte 127 (x1) equals doubling the
+    values of codes 32b..32b+31 of that row, written as e4m3 codes (normal
+    codes with exponent field below 14: code + 8 is the double).  One block
+    per row, different blocks in different rows: a scale applied to the wrong
+    32 codes fails."""
+    T, d = 2, 256
+    codes, _, Wq, Wk, Wm, h = _layer_inputs(T=T, d=d, seed=47)
+    rng = np.random.default_rng(13)
+    exp = rng.integers(1, 14, codes.shape)
+    codes = ((codes & 0x80) | (exp << 3) | (codes & 0x07)).astype(np.uint8)  # normal, exponent field 1..13
+    esc = np.full((T, 24, 8), 127, np.uint8)
+    doubled = codes.copy()
+    for t in range(T):
+        for j in range(24):
+            blk = (3 * j + t) % 8
+            esc[t, j, blk] = 128
+            doubled[t, j, 32 * blk:32 * blk + 32] += 8
+    assert np.array_equal(_e4m3_vals(doubled[0, 0, :32]), 2 * _e4m3_vals(codes[0, 0, :32]))
+    want = oracle.layer_gated(doubled, np.ones((T, 24), np.float32), Wq, Wk, Wm, h)
+    got = oracle.layer_gated(codes, esc, Wq, Wk, Wm, h)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+
+
 def test_hash_positions_entry_rows():
     """The explicit-position entry (used for sampled references) against
     windows built here: any order, repeats, every sequence start and a
