@@ -605,8 +605,8 @@ def run_ours(args, rank, world, local_rank):
     host = cfg.host_tables
     layers = args.variant == "layers"
     if layers:  # the per-layer form: layer 0 (module 0) then layer 1 (module 1), per-row gates
-        if host or args.layout == "mx":
-            raise SystemExit("--variant layers runs on HBM tables with fp32 row scales")
+        if host:
+            raise SystemExit("--variant layers runs on HBM tables")
         lw = []
         for m in (0, 1):
             wq = torch.empty((cfg.d, 256), dtype=torch.bfloat16, device=dev)
@@ -752,7 +752,8 @@ def run_ours(args, rank, world, local_rank):
 
     peaks = measured_peaks()
     # algorithmic bytes per token; a layer moves its 24 rows + scales and h once each way
-    kb = ({"layer0": 24 * 260 + 4 * cfg.d, "layer1": 24 * 260 + 4 * cfg.d} if layers
+    row_bytes = 264 if args.layout == "mx" else 260
+    kb = ({"layer0": 24 * row_bytes + 4 * cfg.d, "layer1": 24 * row_bytes + 4 * cfg.d} if layers
           else kernel_bytes_per_token(cfg.d, args.layout))
     if sharded:  # this rank's share of the rows; the fp32 mem is written, exchanged and read
         kb = {"gather": -(-48 * 260 // world), "fuse": 4 * cfg.d}

@@ -421,7 +421,9 @@ __global__ void __launch_bounds__(256, kGate ? 2 : (kMx ? 3 : 4)) gather_kernel(
 // against the token's key-side query u_t = rinv(h_t) h_t W_q W_k^T
 // (layer::query_kernel, twice).
 // Lane (half, c16) holds 16 values of rows 2i + half; a row's sums are reduced
-// over its half-warp; rows that failed the range check get gate 0.
+// over its half-warp; rows that failed the range check get gate 0.  Rows
+// carry one fp32 scale (separate array or inside a 272-byte record) or, as
+// MXFP8-style rows, eight E8M0 block scales.
 
 constexpr int kLayerWidth = 256;  // values per row: the width of one Engram layer's X and query
 
@@ -438,6 +440,10 @@ struct GatedParams {
     HashParams hp;
 };
 
+// kMx: MXFP8-style rows, eight E8M0 block scales at bytes 256..263; lane
+// (half, c16) holds codes 16 c16 .. 16 c16 + 15, all in block c16 / 2, so
+// each lane scales its own partial sums and codes by its block's scale.
+template <bool kMx>
 __global__ void __launch_bounds__(128, 5) gather_gated_kernel(const __grid_constant__ GatedParams P) {
     // For few tiles launched as a programmatic dependent of the key-side query
     // kernel, whose output u is read only after grid_dependency_wait below: the
@@ -468,21 +474,40 @@ __global__ void __launch_bounds__(128, 5) gather_gated_kernel(const __grid_const
         if (ok) {
             const int64_t flat = (int64_t)j * P.R + r;
             off = flat * P.row_stride;
-            sc = P.scales ? __ldg(P.scales + flat) : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
+            if (!kMx)
+                sc = P.scales ? __ldg(P.scales + flat)
+                              : __ldg(reinterpret_cast<const float *>(P.rows + off + kRowBytes));
         }
     }
     const int half = lane >> 4;
     const int c16 = lane & 15;
     uint4 v[12];
-    float s[12];
+    float s[12];  // the row's scale, or with kMx this lane's block scale of the row
     uint32_t live = 0;  // bit i: row 2i + half passed the range check
+    uint2 tail = make_uint2(0u, 0u);
+    if (kMx) {  // lanes 0..11 of each half-warp: the 8 scale bytes of row 2 c16 + half
+        const int src = 2 * (c16 < 12 ? c16 : 11) + half;
+        const int64_t o = __shfl_sync(0xffffffffu, off, src);
+        const int okt = __shfl_sync(0xffffffffu, ok, src);
+        if (c16 < 12 && okt) tail = __ldg(reinterpret_cast<const uint2 *>(P.rows + o + kRowBytes));
+    }
 #pragma unroll
     for (int i = 0; i < 12; ++i) {
         const int src = 2 * i + half;
         const int64_t o = __shfl_sync(0xffffffffu, off, src);
-        s[i] = __shfl_sync(0xffffffffu, sc, src);
-        v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);
+        if (!kMx) s[i] = __shfl_sync(0xffffffffu, sc, src);
+        v[i] = ld_nc_na_v4(P.rows + o + c16 * 16);  // an invalid row reads row offset 0 and gets gate 0
         if (__shfl_sync(0xffffffffu, ok, src)) live |= 1u << i;
+    }
+    if (kMx) {
+        const int blk = c16 >> 1;
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+            const int L = half * 16 + i;  // the lane holding row 2 i + half's scale bytes
+            const uint32_t x = __shfl_sync(0xffffffffu, tail.x, L);
+            const uint32_t y = __shfl_sync(0xffffffffu, tail.y, L);
+            s[i] = e8m0_to_float(((blk < 4 ? x : y) >> (8 * (blk & 3))) & 0xFFu);
+        }
     }
     grid_dependency_wait();  // u (P.q) is the previous kernel's output
     float qv[16];
@@ -522,13 +547,18 @@ __global__ void __launch_bounds__(128, 5) gather_gated_kernel(const __grid_const
             dd2 = fma2(c[k], u2[k], dd2);
         }
         float ss = ss2.x + ss2.y, dd = dd2.x + dd2.y;
+        const float sc = s[i];
+        if (kMx) {  // this lane's codes carry their block's scale
+            ss *= sc * sc;
+            dd *= sc;
+        }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) {  // over the 16 lanes of this half-warp
             ss += __shfl_xor_sync(0xffffffffu, ss, o);
             dd += __shfl_xor_sync(0xffffffffu, dd, o);
         }
-        const float sc = s[i];
-        const float score = rsqrtf(sc * sc * ss * (1.f / 256.f) + P.eps) * sc * dd * (1.f / 16.f);
+        const float score = kMx ? rsqrtf(ss * (1.f / 256.f) + P.eps) * dd * (1.f / 16.f)
+                                : rsqrtf(sc * sc * ss * (1.f / 256.f) + P.eps) * sc * dd * (1.f / 16.f);
         const float gs = (live >> i) & 1u ? sc / (1.f + __expf(-score)) : 0.f;
         const float2 g2 = make_float2(gs, gs);
 #pragma unroll
@@ -2011,7 +2041,6 @@ extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t 
                                               uint16_t *h, void *workspace, size_t workspace_bytes, void *stream) {
     if (check_config(cfg) != ENGRAM_OK || module < 0 || module > 1 || n_query < 0 || n_seqs < 0 || last_n < 0)
         return ENGRAM_EINVAL;
-    if (mx(cfg)) return ENGRAM_EUNSUPPORTED;
     if (n_query == 0) return ENGRAM_OK;
     if (!tokens || !seq_offsets || n_seqs < 1 || !tables || !scales_ok(cfg, scales) || !W_q || !W_kk || !W_m ||
         !h || !workspace)
@@ -2075,7 +2104,8 @@ extern "C" engram_status engram_layer_forward(const engram_config *cfg, int32_t 
         lc.stream = st;
         lc.attrs = attr;
         lc.numAttrs = query_splits(m_tiles, d) > 1 ? 1 : 0;
-        const cudaError_t le = cudaLaunchKernelEx(&lc, gather_gated_kernel, P);
+        const cudaError_t le = mx(cfg) ? cudaLaunchKernelEx(&lc, gather_gated_kernel<true>, P)
+                                       : cudaLaunchKernelEx(&lc, gather_gated_kernel<false>, P);
         if (le != cudaSuccess) return cuda_fail(le, "cudaLaunchKernelEx(gather_gated)");
     }
     s = launch_status();

@@ -331,8 +331,9 @@ engram_status engram_forward_host(const engram_config *cfg, const int32_t *token
  * engram_layer_keys: W_kk [512][256] = [W_k^T ; W_k^T] (bf16 copies) from
  *   W_k [256][256] (bf16, device); once per set of weights.
  * engram_layer_forward: one layer, in place on h [n_query][d] bf16, from the
- *   HBM tables (ENGRAM_ROWS_SEPARATE or ENGRAM_ROWS_RECORD; MX rows are
- *   ENGRAM_EUNSUPPORTED), W_q [d][256], W_kk and W_m [256][d] (bf16, device).
+ *   HBM tables (any row layout; with ENGRAM_ROWS_MX each code of r_j is scaled
+ *   by its 32-code block's E8M0 scale before the rmsnorm, the dot product and
+ *   the sum), W_q [d][256], W_kk and W_m [256][d] (bf16, device).
  *   Kernels: q = rinv(h) h W_q (tcgen05, written as bf16 q_hi | q_lo), u =
  *   [q_hi | q_lo] W_kk = q W_k^T (tcgen05), the gated gather (hash, gather,
  *   score_j = <u, rmsnorm(r_j)> / 16, X = bf16 [n][256]), the projection.
