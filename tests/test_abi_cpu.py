@@ -158,7 +158,8 @@ def test_layer_entry_points_check_arguments_before_device_work(eg):
     assert fwd(c, n_seqs=2, last_n=1, n_query=4) == 1   # n_query != n_seqs * last_n
     assert fwd(c, ws_bytes=16) == 6                     # workspace too small
     c_mx = eg.make_config(1024, 4096, 256, default_seeds(), row_layout=eg.ROWS_MX)
-    assert fwd(c_mx) == 7                               # MX rows: not in the per-layer form
+    assert fwd(c_mx, ws_bytes=16) == 6                  # MX rows: checked the same way (no device work)
+    assert fwd(c_mx, module=2) == 1
     c_d = eg.make_config(1024, 4096, 320, default_seeds())
     assert fwd(c_d) == 1                                # d not a multiple of 256
 
