@@ -173,6 +173,28 @@ def test_layers_match_oracle(eg, name):
         assert np.all(err <= 1e-3 * bounds[0] + 2.0**-8 * np.abs(es[0]) + 1e-30), (m, float(err.max()))
 
 
+@pytest.mark.parametrize("n", [1, 129, 257])
+def test_layers_at_tile_boundaries(eg, n):
+    """The per-layer form on 1 token, two tiles with a one-token tail, and
+    three tiles with a one-token tail (d = 4096: the split-K query products
+    and the d-split or cluster projection), both layers against the oracle on
+    every token."""
+    cfg = CONFIGS["prefill"].with_(seq_lens=(n,), R=1 << 16, seed=40 + n)
+    w = Workload(cfg)
+    q = np.arange(n)
+    qt = torch.from_numpy(q).cuda()
+    h = w.fresh_h()
+    for m in (0, 1):
+        h_before = _bits(h)
+        wq, wk, wm = _weights(eg, cfg, m)
+        eg.engram_layer_forward(w.c, m, w.tokens, w.seq_offsets, w.tables, w.scales, wq,
+                                eg.engram_layer_keys(w.c, wk), wm, h)
+        torch.cuda.synchronize()
+        assert eg.engram_last_error() == 0
+        ref_h, _, _ = _oracle_layers(w, q, modules=(m,), h_in=h_before)
+        check_h(h[qt], ref_h)
+
+
 def test_layers_many_tiles_persistent_loop(eg):
     """41,000 tokens at d = 4096 (321 tiles of 128, more than twice the SM
     count): the query kernels (grid = min(tiles, SMs)) and the ungated

@@ -283,6 +283,23 @@ def test_dependent_forward_steps_in_one_graph(eg, name):
     assert torch.equal(h_eager.view(torch.int16), h_graph.view(torch.int16))
 
 
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 255, 256, 257, 1153])
+def test_forward_at_tile_boundaries(eg, n):
+    """Batches of 1 token, one tile less / exactly / one more, two tiles and
+    three (d = 4096: the d-split kernel up to two tiles, the cluster kernel
+    from three) and a tail of one token after nine tiles: engram_forward
+    against the oracle on every token, and equal to the split form's bits."""
+    w = Workload(CONFIGS["prefill"].with_(seq_lens=(n,), R=1 << 16, seed=20 + n))
+    h1, h2 = w.fresh_h(), w.fresh_h()
+    eg.engram_forward(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h1)
+    X = eg.engram_gather_x(w.c, w.tokens, w.seq_offsets, w.tables, w.scales)
+    eg.engram_fuse_x(w.c, X, w.W, w.g, h2)
+    _clear(eg)
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    _, _, _, ref_h, _ = w.ref_for(np.arange(n))
+    check_h(h1, ref_h)
+
+
 def test_generator_twin_rows_match_host(eg):
     """The device-filled tables/scales/h equal the host draws bit for bit."""
     cfg = SMALL["ragged_prime"]
