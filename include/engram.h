@@ -388,7 +388,10 @@ engram_status engram_host_free(void *ptr);
  * h equals engram_forward's on the same tables bit for bit.
  *   stamp    >= 1, larger than every earlier call's on this cache since its
  *            reset (a call counter); a cache serves one stream of calls:
- *            calls that overlap on the GPU race on it
+ *            calls that overlap on the GPU race on it.  A call captured in a
+ *            CUDA graph replays its stamp: replays after the first find every
+ *            slot claimed at that stamp and stage all their rows into the
+ *            overflow area (no hits), with h still bit-exact
  *   capacity distinct rows per call at most (n_query * 48 always suffices);
  *            more set ENGRAM_ECAPACITY, stage nothing and leave h unchanged
  *   stats    int64 [4] (device): distinct rows, cache hits, rows staged over

@@ -79,3 +79,47 @@ def test_cached_capacity_overflow_leaves_h(eg):
     torch.cuda.synchronize()
     assert eg.engram_last_error() == 4  # ENGRAM_ECAPACITY
     assert torch.equal(h.view(torch.int16), h0.view(torch.int16))
+
+
+def test_cached_call_in_cuda_graph(eg):
+    """A call captured in a CUDA graph replays its stamp.  The first replay
+    (a newer stamp than the eager call before it) is served from the rows
+    that call cached; the second finds every slot already claimed at its own
+    stamp and stages every row into the overflow area (no hits).  h equals the
+    HBM path's bits after every call."""
+    w = Workload(CFG, host_tables=True)
+    cap, slots = CFG.tq * 48, 1 << 20
+    cache = eg.engram_host_cache_new(w.c, slots, cap)
+    dev_t, dev_s = w.tables.cuda(), w.scales.cuda()
+    side, s = torch.cuda.Stream(), torch.cuda.Stream()
+    ws = torch.empty(eg.engram_forward_host_cached_workspace_bytes(w.c, CFG.tq, cap), dtype=torch.uint8,
+                     device="cuda")
+    stats = torch.zeros(4, dtype=torch.int64, device="cuda")
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def call(h, stamp):
+        eg.engram_forward_host_cached(w.c, w.tokens, w.seq_offsets, w.tables, w.scales, w.W, w.g, h, cache, slots,
+                                      cap, stamp=stamp, workspace=ws, stats=stats, stream=s, side_stream=side,
+                                      ev_dedup=evs[0], ev_staged=evs[1])
+
+    h, ref = w.fresh_h(), w.fresh_h()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        call(h, 1)
+    for _ in range(3):
+        eg.engram_forward(w.c, w.tokens, w.seq_offsets, dev_t, dev_s, w.W, w.g, ref)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call(h, 2)
+    graph.replay()
+    torch.cuda.synchronize()
+    st1 = stats.cpu().numpy().copy()
+    graph.replay()
+    torch.cuda.synchronize()
+    st2 = stats.cpu().numpy().copy()
+    assert eg.engram_last_error() == 0
+    assert torch.equal(h.view(torch.int16), ref.view(torch.int16))
+    U = st1[0]
+    assert st1[1] >= 0.9 * U and st1[1] + st1[2] == U
+    assert st2[0] == U and st2[1] == 0 and st2[2] == U and st2[3] == U
